@@ -261,9 +261,11 @@ def moe_forward(x, logits, get_w1, get_w2, k, gs_h, tokens=None, keep=False):
     pre-computed global scale of the intermediate activation (README "Bridge
     Layer": quantize_activation_nvfp4 with pre-computed gs).
 
-    Returns a dict with the routing, the permutation, gs_x, and for each listed
-    token its output row y (fp64), plus per-(token, j) intermediates when
-    ``keep`` is set.
+    Routing, permutation and gs_x always cover all T tokens; the expert work is
+    done for the listed tokens only, one expert at a time (so only one expert's
+    dequantized weights are held in memory). Returns a dict with the routing,
+    the permutation, gs_x, y (len(tokens), K) fp64, and per-(token, j)
+    intermediates when ``keep`` is set.
     """
     T, K = x.shape
     E = logits.shape[1]
@@ -271,34 +273,35 @@ def moe_forward(x, logits, get_w1, get_w2, k, gs_h, tokens=None, keep=False):
     offsets, p2f, f2p = permute(ids, E)
     amax_x = amax_bf16(x)
     gs_x = global_scale(amax_x)
-    if tokens is None:
-        tokens = list(range(T))
-    cache = {}
-
-    def expert(e):
-        if e not in cache:
-            c1, s1, g1 = quantize_expert(get_w1(e))
-            c2, s2, g2 = quantize_expert(get_w2(e))
-            cache[e] = (dequantize_f64(c1, s1, g1), dequantize_f64(c2, s2, g2), g1, g2,
-                        (c1, s1, c2, s2))
-        return cache[e]
-
-    y = np.zeros((len(tokens), K), np.float64)
-    inter = {}
+    tokens = list(range(T)) if tokens is None else [int(t) for t in tokens]
+    xc, xs = quantize_bf16(np.ascontiguousarray(x[tokens]), gs_x)
+    xd = dequantize_f64(xc, xs, gs_x)
+    by_expert = {}
     for ti, t in enumerate(tokens):
-        xc, xs = quantize_bf16(x[t:t + 1], gs_x)
-        a = dequantize_f64(xc, xs, gs_x)
         for j in range(k):
-            e = int(ids[t, j])
-            d1, d2, _, _, _ = expert(e)
-            v = matmul_nt(a, d1)                  # (1, 2I): [gate | up]
-            h = swiglu(v)                         # (1, I) f32
-            hc, hs = quantize_f32(h, gs_h)
-            hd = dequantize_f64(hc, hs, gs_h)
-            o = matmul_nt(hd, d2)                 # (1, K)
-            y[ti] += w[t, j] * o[0]
+            by_expert.setdefault(int(ids[t, j]), []).append((ti, j))
+    outs = np.zeros((len(tokens), k, K), np.float64)
+    inter = {}
+    gs_w = {}
+    for e in sorted(by_expert):
+        c1, s1, g1 = quantize_expert(get_w1(e))
+        c2, s2, g2 = quantize_expert(get_w2(e))
+        gs_w[e] = (g1, g2)
+        pairs = by_expert[e]
+        a = xd[[ti for ti, _ in pairs]]
+        v = matmul_nt(a, dequantize_f64(c1, s1, g1))          # (n, 2I): [gate | up]
+        h = swiglu(v)                                          # (n, I) f32
+        hc, hs = quantize_f32(h, gs_h)
+        o = matmul_nt(dequantize_f64(hc, hs, gs_h), dequantize_f64(c2, s2, g2))
+        for r, (ti, j) in enumerate(pairs):
+            outs[ti, j] = o[r]
             if keep:
-                inter[(t, j)] = dict(xc=xc, xs=xs, v=v, h=h, hc=hc, hs=hs, o=o[0])
+                inter[(tokens[ti], j)] = dict(v=v[r], h=h[r], hc=hc[r], hs=hs[r], o=o[r])
+    # step 6: weighted sum over j, in j order, fp64
+    y = np.zeros((len(tokens), K), np.float64)
+    wt = w[tokens]
+    for j in range(k):
+        y += wt[:, j:j + 1] * outs[:, j]
     return dict(ids=ids, w=w, offsets=offsets, perm_to_flat=p2f, flat_to_perm=f2p,
-                amax_x=amax_x, gs_x=gs_x, tokens=list(tokens), y=y, inter=inter,
-                experts={e: (v[2], v[3], v[4]) for e, v in cache.items()})
+                amax_x=amax_x, gs_x=gs_x, tokens=tokens, x_codes=xc, x_sf=xs, y=y,
+                inter=inter, gs_w=gs_w)

@@ -119,6 +119,35 @@ float orc_global_scale(float amax) {
   return num / amax;
 }
 
+static int g_threads = 0;
+
+void orc_set_threads(int n) { g_threads = n; }
+
+int orc_get_threads() {
+  if (g_threads > 0) return g_threads;
+  unsigned h = std::thread::hardware_concurrency();
+  return h ? (int)h : 1;
+}
+
+}  // extern "C"
+
+template <class F>
+static void parallel_rows(int64_t rows, F fn) {
+  int nt = (int)std::min<int64_t>(orc_get_threads(), std::max<int64_t>(rows, 1));
+  if (nt <= 1) {
+    for (int64_t r = 0; r < rows; ++r) fn(r);
+    return;
+  }
+  std::vector<std::thread> th;
+  for (int i = 0; i < nt; ++i)
+    th.emplace_back([&, i] {
+      for (int64_t r = i; r < rows; r += nt) fn(r);
+    });
+  for (auto& t : th) t.join();
+}
+
+extern "C" {
+
 static inline float bf16_to_f32(uint16_t b) {
   uint32_t u = (uint32_t)b << 16;
   float f;
@@ -176,21 +205,23 @@ static uint8_t quantize_block(const float* v, float gs, uint8_t* out8) {
 // codes: rows x cols/2 bytes, row-major. sf: rows x cols/16 bytes, row-major.
 void orc_quantize_bf16(const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx, float gs,
                        uint8_t* codes, uint8_t* sf) {
-  float blk[16];
-  for (int64_t r = 0; r < rows; ++r)
+  parallel_rows(rows, [&](int64_t r) {
+    float blk[16];
     for (int64_t b = 0; b < cols / 16; ++b) {
       for (int i = 0; i < 16; ++i) blk[i] = bf16_to_f32(x[r * ldx + b * 16 + i]);
       sf[r * (cols / 16) + b] = quantize_block(blk, gs, codes + r * (cols / 2) + b * 8);
     }
+  });
 }
 
 // Same for f32 input (the requantization of h, and the round-trip identity).
 void orc_quantize_f32(const float* x, int64_t rows, int64_t cols, float gs, uint8_t* codes,
                       uint8_t* sf) {
-  for (int64_t r = 0; r < rows; ++r)
+  parallel_rows(rows, [&](int64_t r) {
     for (int64_t b = 0; b < cols / 16; ++b)
       sf[r * (cols / 16) + b] =
           quantize_block(x + r * cols + b * 16, gs, codes + r * (cols / 2) + b * 8);
+  });
 }
 
 // R7 in f32 (used for the byte round-trip of README bug 2): v = (code*s)/gs.
@@ -209,13 +240,14 @@ void orc_dequantize_f32(const uint8_t* codes, const uint8_t* sf, int64_t rows, i
 // R7 in fp64.
 void orc_dequantize_f64(const uint8_t* codes, const uint8_t* sf, int64_t rows, int64_t cols,
                         float gs, double* out) {
-  for (int64_t r = 0; r < rows; ++r)
+  parallel_rows(rows, [&](int64_t r) {
     for (int64_t c = 0; c < cols; ++c) {
       uint8_t byte = codes[r * (cols / 2) + c / 2];
       uint8_t code = (c & 1) ? (byte >> 4) : (byte & 15);
       double s = orc_e4m3_decode(sf[r * (cols / 16) + c / 16]);
       out[r * cols + c] = orc_e2m1_decode(code) * s / (double)gs;
     }
+  });
 }
 
 // ---------------------------------------------------------------- layout
@@ -280,34 +312,7 @@ void orc_permute(const int32_t* ids, int64_t T, int k, int E, int32_t* offsets,
 
 // ---------------------------------------------------------------- GEMM
 
-static int g_threads = 0;
 
-void orc_set_threads(int n) { g_threads = n; }
-
-int orc_get_threads() {
-  if (g_threads > 0) return g_threads;
-  unsigned h = std::thread::hardware_concurrency();
-  return h ? (int)h : 1;
-}
-
-}  // extern "C"
-
-template <class F>
-static void parallel_rows(int64_t rows, F fn) {
-  int nt = (int)std::min<int64_t>(orc_get_threads(), std::max<int64_t>(rows, 1));
-  if (nt <= 1) {
-    for (int64_t r = 0; r < rows; ++r) fn(r);
-    return;
-  }
-  std::vector<std::thread> th;
-  for (int i = 0; i < nt; ++i)
-    th.emplace_back([&, i] {
-      for (int64_t r = i; r < rows; r += nt) fn(r);
-    });
-  for (auto& t : th) t.join();
-}
-
-extern "C" {
 
 // C[r][n] = sum_k A[r][k] * B[n][k], fp64, plain loops (threads over rows).
 void orc_matmul_nt(const double* A, const double* B, int64_t M, int64_t N, int64_t K, double* C) {

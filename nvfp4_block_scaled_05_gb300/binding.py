@@ -1,0 +1,296 @@
+"""Thin Python binding of libnvfp4moe.so (the C ABI in include/nvfp4moe.h).
+
+Every function here has the name of the C entry point it calls and only
+marshals arguments: it allocates outputs with torch (device memory is the one
+thing torch is used for), passes raw pointers and torch's current stream, and
+raises on a non-zero status. All arithmetic runs in the library's kernels; if
+the library cannot be loaded, every call fails loudly.
+"""
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+NVFP4_SF_ROWMAJOR = 0
+NVFP4_SF_TILED = 1
+
+_c_void_p = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_int = ctypes.c_int
+_size = ctypes.c_size_t
+
+_SIGS = {
+    "nvfp4moe_status_string": (ctypes.c_char_p, [_int]),
+    "nvfp4_sf_bytes": (_size, [_i64, _i64, _int]),
+    "nvfp4moe_padded_rows": (_i64, [_i64, _int]),
+    "nvfp4moe_interleave_row_map": (_int, [_i64, _c_void_p]),
+    "nvfp4_quantize_workspace_size": (_size, []),
+    "nvfp4_quantize": (_int, [_c_void_p, _i64, _i64, _i64, _c_void_p, _c_void_p, _c_void_p,
+                              _c_void_p, _c_void_p, _int, _c_void_p, _size, _c_void_p]),
+    "moe_route_topk": (_int, [_c_void_p, _i64, _int, _int, _c_void_p, _c_void_p, _c_void_p]),
+    "moe_permute_workspace_size": (_size, [_i64, _int, _int]),
+    "moe_permute": (_int, [_c_void_p, _i64, _int, _int, _c_void_p, _c_void_p, _c_void_p,
+                           _c_void_p, _size, _c_void_p]),
+    "moe_quantize_dispatch_workspace_size": (_size, [_int]),
+    "moe_quantize_dispatch": (_int, [_c_void_p, _i64, _i64, _i64, _int, _int, _c_void_p,
+                                     _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                                     _c_void_p, _i64, _c_void_p, _size, _c_void_p]),
+    "nvfp4_grouped_gemm": (_int, [_c_void_p, _c_void_p, _c_void_p, _i64, _c_void_p, _c_void_p,
+                                  _c_void_p, _c_void_p, _int, _i64, _i64, _c_void_p, _i64,
+                                  _c_void_p]),
+    "nvfp4_grouped_gemm_swiglu": (_int, [_c_void_p, _c_void_p, _c_void_p, _i64, _c_void_p,
+                                         _c_void_p, _c_void_p, _c_void_p, _int, _i64, _i64,
+                                         _c_void_p, _c_void_p, _c_void_p, _c_void_p]),
+    "moe_combine": (_int, [_c_void_p, _i64, _c_void_p, _c_void_p, _i64, _int, _i64, _c_void_p,
+                           _i64, _c_void_p]),
+    "moe_forward_workspace_size": (_size, [_i64, _i64, _i64, _int, _int]),
+    "moe_forward_workspace_layout": (_int, [_i64, _i64, _i64, _int, _int, _c_void_p]),
+    "moe_forward": (_int, [_c_void_p, _c_void_p, _i64, _i64, _i64, _int, _int, _c_void_p,
+                           _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                           _c_void_p, _c_void_p, _size, _c_void_p]),
+    "nvfp4moe_last_device_status": (_int, [_c_void_p]),
+    "nvfp4moe_set_wait_limit_ns": (None, [ctypes.c_uint64]),
+    "nvfp4moe_num_sms": (_int, []),
+}
+
+_lib = None
+
+
+class NVFP4Error(RuntimeError):
+    pass
+
+
+def lib():
+    """Load (building first if stale) the in-tree libnvfp4moe.so."""
+    global _lib
+    if _lib is None:
+        path = _build.LIB if os.path.exists(_build.LIB) and not _build.stale() else _build.build()
+        L = ctypes.CDLL(path)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _check(status, what):
+    if status != 0:
+        msg = lib().nvfp4moe_status_string(status).decode()
+        raise NVFP4Error("%s failed: %s (%d)" % (what, msg, status))
+
+
+def _dev(t, name):
+    if not (isinstance(t, torch.Tensor) and t.is_cuda):
+        raise NVFP4Error("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise NVFP4Error("%s must be contiguous" % name)
+    return t
+
+
+# ------------------------------------------------------------------ sizes
+
+def nvfp4_sf_bytes(rows, cols, sf_layout=NVFP4_SF_TILED):
+    return int(lib().nvfp4_sf_bytes(rows, cols, sf_layout))
+
+
+def nvfp4moe_padded_rows(M, E):
+    return int(lib().nvfp4moe_padded_rows(M, E))
+
+
+def nvfp4moe_interleave_row_map(two_i):
+    m = (ctypes.c_int32 * two_i)()
+    _check(lib().nvfp4moe_interleave_row_map(two_i, ctypes.cast(m, ctypes.c_void_p)), "interleave_row_map")
+    return torch.tensor(list(m), dtype=torch.int32)
+
+
+def nvfp4moe_num_sms():
+    return int(lib().nvfp4moe_num_sms())
+
+
+def nvfp4moe_last_device_status():
+    return int(lib().nvfp4moe_last_device_status(_stream()))
+
+
+def nvfp4moe_set_wait_limit_ns(ns):
+    lib().nvfp4moe_set_wait_limit_ns(int(ns))
+
+
+def moe_forward_workspace_size(T, K, I, E, k):
+    return int(lib().moe_forward_workspace_size(T, K, I, E, k))
+
+
+def moe_forward_workspace_layout(T, K, I, E, k):
+    offs = (ctypes.c_int64 * 12)()
+    _check(lib().moe_forward_workspace_layout(T, K, I, E, k, ctypes.cast(offs, ctypes.c_void_p)),
+           "moe_forward_workspace_layout")
+    names = ["topk_ids", "topk_w", "offsets", "perm_to_flat", "flat_to_perm", "gs_x", "a_codes",
+             "a_sf", "h_codes", "h_sf", "out", "a_rows"]
+    return dict(zip(names, list(offs)))
+
+
+# ------------------------------------------------------------------ ops
+
+def nvfp4_quantize(x, gs=None, row_src=None, sf_layout=NVFP4_SF_TILED, rows=None,
+                   codes=None, sf=None, gs_out=None):
+    """BF16 (rows, cols) -> (codes, sf, gs). gs: device f32 tensor or None (computed)."""
+    _dev(x, "x")
+    assert x.dtype == torch.bfloat16 and x.dim() == 2
+    cols = x.shape[1]
+    if rows is None:
+        rows = row_src.numel() if row_src is not None else x.shape[0]
+    dev = x.device
+    if codes is None:
+        codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device=dev)
+    if sf is None:
+        sf = torch.empty(nvfp4_sf_bytes(rows, cols, sf_layout), dtype=torch.uint8, device=dev)
+    if gs_out is None:
+        gs_out = torch.empty(1, dtype=torch.float32, device=dev)
+    ws = None
+    ws_bytes = 0
+    if gs is None:
+        ws_bytes = int(lib().nvfp4_quantize_workspace_size())
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    _check(lib().nvfp4_quantize(_ptr(x), rows, cols, x.stride(0), _ptr(gs), _ptr(gs_out),
+                                _ptr(row_src), _ptr(codes), _ptr(sf), sf_layout, _ptr(ws), ws_bytes,
+                                _stream()), "nvfp4_quantize")
+    return codes, sf, gs_out
+
+
+def moe_route_topk(logits, k):
+    _dev(logits, "logits")
+    T, E = logits.shape
+    ids = torch.empty((T, k), dtype=torch.int32, device=logits.device)
+    w = torch.empty((T, k), dtype=torch.float32, device=logits.device)
+    _check(lib().moe_route_topk(_ptr(logits), T, E, k, _ptr(ids), _ptr(w), _stream()), "moe_route_topk")
+    return ids, w
+
+
+def moe_permute(topk_ids, E):
+    _dev(topk_ids, "topk_ids")
+    T, k = topk_ids.shape
+    dev = topk_ids.device
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    p2f = torch.empty(T * k, dtype=torch.int32, device=dev)
+    f2p = torch.empty(T * k, dtype=torch.int32, device=dev)
+    nb = int(lib().moe_permute_workspace_size(T, k, E))
+    ws = torch.empty(max(nb, 1), dtype=torch.uint8, device=dev)
+    _check(lib().moe_permute(_ptr(topk_ids), T, k, E, _ptr(offsets), _ptr(p2f), _ptr(f2p), _ptr(ws),
+                             nb, _stream()), "moe_permute")
+    return offsets, p2f, f2p
+
+
+def moe_quantize_dispatch(x, topk_ids, offsets, flat_to_perm, E, gs=None, a_rows=None):
+    _dev(x, "x")
+    T, K = x.shape
+    k = topk_ids.shape[1]
+    dev = x.device
+    if a_rows is None:
+        a_rows = nvfp4moe_padded_rows(T * k, E)
+    a_codes = torch.zeros((a_rows, K // 2), dtype=torch.uint8, device=dev)
+    a_sf = torch.zeros(nvfp4_sf_bytes(a_rows, K), dtype=torch.uint8, device=dev)
+    gs_out = torch.empty(1, dtype=torch.float32, device=dev)
+    nb = int(lib().moe_quantize_dispatch_workspace_size(E))
+    ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+    _check(lib().moe_quantize_dispatch(_ptr(x), T, K, x.stride(0), k, E, _ptr(topk_ids), _ptr(offsets),
+                                       _ptr(flat_to_perm), _ptr(gs), _ptr(gs_out), _ptr(a_codes),
+                                       _ptr(a_sf), a_rows, _ptr(ws), nb, _stream()),
+           "moe_quantize_dispatch")
+    return a_codes, a_sf, gs_out
+
+
+def nvfp4_grouped_gemm(a_codes, a_sf, gs_a, b_codes, b_sf, gs_b, offsets, out=None):
+    """A grouped-padded (a_rows, K/2); B (E, N, K/2) -> C (M, N) BF16, compact rows."""
+    E, N, khalf = b_codes.shape
+    K = khalf * 2
+    M = None
+    if out is None:
+        M = int(offsets[-1].item())
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=a_codes.device)
+    _check(lib().nvfp4_grouped_gemm(_ptr(a_codes), _ptr(a_sf), _ptr(gs_a), a_codes.shape[0],
+                                    _ptr(b_codes), _ptr(b_sf), _ptr(gs_b), _ptr(offsets), E, N, K,
+                                    _ptr(out), out.stride(0), _stream()), "nvfp4_grouped_gemm")
+    return out
+
+
+def nvfp4_grouped_gemm_swiglu(a_codes, a_sf, gs_a, w1_codes, w1_sf, gs_w1, offsets, gs_h,
+                              h_codes=None, h_sf=None):
+    E, two_i, khalf = w1_codes.shape
+    K, I = khalf * 2, two_i // 2
+    a_rows = a_codes.shape[0]
+    dev = a_codes.device
+    if h_codes is None:
+        h_codes = torch.zeros((a_rows, I // 2), dtype=torch.uint8, device=dev)
+    if h_sf is None:
+        h_sf = torch.zeros(nvfp4_sf_bytes(a_rows, I), dtype=torch.uint8, device=dev)
+    _check(lib().nvfp4_grouped_gemm_swiglu(_ptr(a_codes), _ptr(a_sf), _ptr(gs_a), a_rows,
+                                           _ptr(w1_codes), _ptr(w1_sf), _ptr(gs_w1), _ptr(offsets), E,
+                                           I, K, _ptr(gs_h), _ptr(h_codes), _ptr(h_sf), _stream()),
+           "nvfp4_grouped_gemm_swiglu")
+    return h_codes, h_sf
+
+
+def moe_combine(out, topk_w, flat_to_perm, y=None):
+    T, k = topk_w.shape
+    K = out.shape[1]
+    if y is None:
+        y = torch.empty((T, K), dtype=torch.bfloat16, device=out.device)
+    _check(lib().moe_combine(_ptr(out), out.stride(0), _ptr(topk_w), _ptr(flat_to_perm), T, k, K,
+                             _ptr(y), y.stride(0), _stream()), "moe_combine")
+    return y
+
+
+def moe_forward(x, logits, weights, k, gs_h, ws=None, y=None):
+    """The whole expert forward; weights from prepare_moe_weights()."""
+    T, K = x.shape
+    E = logits.shape[1]
+    I = weights["I"]
+    nb = moe_forward_workspace_size(T, K, I, E, k)
+    if ws is None:
+        ws = torch.empty(nb, dtype=torch.uint8, device=x.device)
+    if y is None:
+        y = torch.empty((T, K), dtype=torch.bfloat16, device=x.device)
+    _check(lib().moe_forward(_ptr(x), _ptr(logits), T, K, I, E, k, _ptr(weights["w1_codes"]),
+                             _ptr(weights["w1_sf"]), _ptr(weights["gs_w1"]), _ptr(weights["w2_codes"]),
+                             _ptr(weights["w2_sf"]), _ptr(weights["gs_w2"]), _ptr(gs_h), _ptr(y),
+                             _ptr(ws), ws.numel(), _stream()), "moe_forward")
+    return y
+
+
+def prepare_moe_weights(w1, w2, free_source=False):
+    """Offline weight preparation through nvfp4_quantize (README "Bridge Layer":
+    quantize_weight_to_nvfp4, interleave_l1_weights, make_b_k_major).
+
+    w1: (E, 2I, K) BF16 rows [gate | up]; w2: (E, K, I) BF16. Each expert gets
+    its own global scale; W1 rows are gathered into the granularity-8
+    interleaved order by the quantizer's row map.
+    """
+    E, two_i, K = w1.shape
+    I = two_i // 2
+    dev = w1.device
+    rmap = nvfp4moe_interleave_row_map(two_i).to(dev)
+    out = {"E": E, "I": I, "K": K}
+    out["w1_codes"] = torch.empty((E, two_i, K // 2), dtype=torch.uint8, device=dev)
+    sf1 = nvfp4_sf_bytes(two_i, K)
+    out["w1_sf"] = torch.empty(E * sf1, dtype=torch.uint8, device=dev)
+    out["gs_w1"] = torch.empty(E, dtype=torch.float32, device=dev)
+    out["w2_codes"] = torch.empty((E, K, I // 2), dtype=torch.uint8, device=dev)
+    sf2 = nvfp4_sf_bytes(K, I)
+    out["w2_sf"] = torch.empty(E * sf2, dtype=torch.uint8, device=dev)
+    out["gs_w2"] = torch.empty(E, dtype=torch.float32, device=dev)
+    for e in range(E):
+        nvfp4_quantize(w1[e], row_src=rmap, codes=out["w1_codes"][e],
+                       sf=out["w1_sf"][e * sf1:(e + 1) * sf1], gs_out=out["gs_w1"][e:e + 1])
+        nvfp4_quantize(w2[e], codes=out["w2_codes"][e], sf=out["w2_sf"][e * sf2:(e + 1) * sf2],
+                       gs_out=out["gs_w2"][e:e + 1])
+    return out

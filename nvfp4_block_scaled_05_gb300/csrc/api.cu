@@ -1,0 +1,148 @@
+// Host-side entry points: sizes and layouts, and moe_forward, which enqueues
+// the six stages of the "NVFP4 MegaMoE Kernel" README "MoE Runner" (with the
+// fused L1 of "Fused SwiGLU - How It Works") on one stream.
+#include "common.cuh"
+
+using namespace nvfp4moe;
+
+extern "C" const char* nvfp4moe_status_string(int status) {
+  switch (status) {
+    case NVFP4MOE_OK: return "ok";
+    case NVFP4MOE_ERR_INVALID: return "invalid argument";
+    case NVFP4MOE_ERR_UNSUPPORTED: return "unsupported shape";
+    case NVFP4MOE_ERR_WORKSPACE: return "workspace missing or too small";
+    case NVFP4MOE_ERR_LAUNCH: return "CUDA launch error";
+    case NVFP4MOE_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+extern "C" size_t nvfp4_sf_bytes(int64_t rows, int64_t cols, int sf_layout) {
+  if (rows < 0 || cols < 0) return 0;
+  if (sf_layout == NVFP4_SF_ROWMAJOR) return (size_t)(rows * (cols / 16));
+  if (sf_layout == NVFP4_SF_TILED) return (size_t)(ceil_div(rows, 128) * ceil_div(cols, 64) * 512);
+  return 0;
+}
+
+extern "C" int64_t nvfp4moe_padded_rows(int64_t M, int E) {
+  if (M < 0 || E < 1) return 0;
+  const int64_t groups = M < E ? M : E;
+  const int64_t r = ceil_div(M + groups * 127, 128) * 128;
+  return r > 128 ? r : 128;
+}
+
+extern "C" int nvfp4moe_interleave_row_map(int64_t two_i, int32_t* map_host) {
+  if (two_i <= 0 || two_i % 16 != 0 || !map_host) return NVFP4MOE_ERR_INVALID;
+  const int64_t I = two_i / 2;
+  for (int64_t n = 0; n < I; ++n) {
+    const int64_t base = 16 * (n / 8) + n % 8;
+    map_host[base] = (int32_t)n;          // gate row n
+    map_host[base + 8] = (int32_t)(I + n);  // up row n
+  }
+  return NVFP4MOE_OK;
+}
+
+namespace {
+
+struct Layout {
+  int64_t off[12];
+  int64_t total;
+};
+
+int64_t up256(int64_t v) { return ceil_div(v, 256) * 256; }
+
+// topk_ids, topk_w, offsets, perm_to_flat, flat_to_perm, gs_x, a_codes, a_sf,
+// h_codes, h_sf, out, then the permute and dispatch scratch.
+Layout make_layout(int64_t T, int64_t K, int64_t I, int E, int k) {
+  Layout L{};
+  const int64_t M = T * k;
+  const int64_t a_rows = nvfp4moe_padded_rows(M, E);
+  int64_t o = 0;
+  auto take = [&](int64_t bytes) {
+    const int64_t at = o;
+    o += up256(bytes > 0 ? bytes : 1);
+    return at;
+  };
+  L.off[0] = take(M * 4);
+  L.off[1] = take(M * 4);
+  L.off[2] = take((E + 1) * 4);
+  L.off[3] = take(M * 4);
+  L.off[4] = take(M * 4);
+  L.off[5] = take(4);
+  L.off[6] = take(a_rows * (K / 2));
+  L.off[7] = take((int64_t)nvfp4_sf_bytes(a_rows, K, NVFP4_SF_TILED));
+  L.off[8] = take(a_rows * (I / 2));
+  L.off[9] = take((int64_t)nvfp4_sf_bytes(a_rows, I, NVFP4_SF_TILED));
+  L.off[10] = take(M * K * 2);
+  L.off[11] = a_rows;
+  const int64_t perm_ws = take((int64_t)moe_permute_workspace_size(T, k, E));
+  const int64_t disp_ws = take((int64_t)moe_quantize_dispatch_workspace_size(E));
+  (void)perm_ws;
+  (void)disp_ws;
+  L.total = o;
+  return L;
+}
+
+bool forward_shape_ok(int64_t T, int64_t K, int64_t I, int E, int k) {
+  return T >= 0 && K > 0 && K % 128 == 0 && I > 0 && I % 64 == 0 && k >= 1 && k <= 16 && E >= k &&
+         E <= 1024 && T * k < (1ll << 31);
+}
+
+}  // namespace
+
+extern "C" size_t moe_forward_workspace_size(int64_t T, int64_t K, int64_t I, int E, int k) {
+  if (!forward_shape_ok(T, K, I, E, k)) return 0;
+  return (size_t)make_layout(T, K, I, E, k).total;
+}
+
+extern "C" int moe_forward_workspace_layout(int64_t T, int64_t K, int64_t I, int E, int k,
+                                            int64_t* offs_host) {
+  if (!forward_shape_ok(T, K, I, E, k)) return NVFP4MOE_ERR_UNSUPPORTED;
+  if (!offs_host) return NVFP4MOE_ERR_INVALID;
+  const Layout L = make_layout(T, K, I, E, k);
+  for (int i = 0; i < 12; ++i) offs_host[i] = L.off[i];
+  return NVFP4MOE_OK;
+}
+
+extern "C" int moe_forward(const void* x, const float* router_logits, int64_t T, int64_t K,
+                           int64_t I, int E, int k, const uint8_t* w1_codes, const uint8_t* w1_sf,
+                           const float* gs_w1, const uint8_t* w2_codes, const uint8_t* w2_sf,
+                           const float* gs_w2, const float* gs_h, void* y, void* ws,
+                           size_t ws_bytes, void* stream) {
+  NVFP4_CHECK(forward_shape_ok(T, K, I, E, k), NVFP4MOE_ERR_UNSUPPORTED);
+  if (T == 0) return NVFP4MOE_OK;
+  NVFP4_CHECK(x && router_logits && w1_codes && w1_sf && gs_w1 && w2_codes && w2_sf && gs_w2 &&
+                  gs_h && y,
+              NVFP4MOE_ERR_INVALID);
+  const Layout L = make_layout(T, K, I, E, k);
+  NVFP4_CHECK(ws && ws_bytes >= (size_t)L.total && aligned(ws, 256), NVFP4MOE_ERR_WORKSPACE);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int32_t* ids = reinterpret_cast<int32_t*>(w + L.off[0]);
+  float* topw = reinterpret_cast<float*>(w + L.off[1]);
+  int32_t* offsets = reinterpret_cast<int32_t*>(w + L.off[2]);
+  int32_t* p2f = reinterpret_cast<int32_t*>(w + L.off[3]);
+  int32_t* f2p = reinterpret_cast<int32_t*>(w + L.off[4]);
+  float* gs_x = reinterpret_cast<float*>(w + L.off[5]);
+  uint8_t* a_codes = w + L.off[6];
+  uint8_t* a_sf = w + L.off[7];
+  uint8_t* h_codes = w + L.off[8];
+  uint8_t* h_sf = w + L.off[9];
+  void* out = w + L.off[10];
+  const int64_t a_rows = L.off[11];
+  const int64_t M = T * k;
+  uint8_t* perm_ws = w + L.off[10] + up256(M * K * 2);
+  const size_t perm_bytes = moe_permute_workspace_size(T, k, E);
+  uint8_t* disp_ws = perm_ws + up256((int64_t)perm_bytes);
+  const size_t disp_bytes = moe_quantize_dispatch_workspace_size(E);
+
+  NVFP4_TRY(moe_route_topk(router_logits, T, E, k, ids, topw, stream));
+  NVFP4_TRY(moe_permute(ids, T, k, E, offsets, p2f, f2p, perm_ws, perm_bytes, stream));
+  NVFP4_TRY(moe_quantize_dispatch(x, T, K, K, k, E, ids, offsets, f2p, nullptr, gs_x, a_codes, a_sf,
+                                  a_rows, disp_ws, disp_bytes, stream));
+  NVFP4_TRY(nvfp4_grouped_gemm_swiglu(a_codes, a_sf, gs_x, a_rows, w1_codes, w1_sf, gs_w1, offsets,
+                                      E, I, K, gs_h, h_codes, h_sf, stream));
+  NVFP4_TRY(nvfp4_grouped_gemm(h_codes, h_sf, gs_h, a_rows, w2_codes, w2_sf, gs_w2, offsets, E, K,
+                               I, out, K, stream));
+  NVFP4_TRY(moe_combine(out, K, topw, f2p, T, k, K, y, K, stream));
+  return NVFP4MOE_OK;
+}

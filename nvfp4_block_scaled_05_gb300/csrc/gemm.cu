@@ -1,0 +1,524 @@
+// Persistent NVFP4 grouped GEMM for sm_103a ("NVFP4 MegaMoE Kernel" README,
+// "ScaledGroupedGemmKernel": A(M,K) x B(E,K,N) -> C(M,N), block-scaled on both
+// operands, per-expert global scales, persistent scheduler, TMA pipelining,
+// swizzled shared memory; and "Fused SwiGLU - How It Works" for the L1
+// epilogue, extended with "Remaining Steps" 2-4: NVFP4 requantization in the
+// epilogue, FP4 codes and scales stored straight into the padded L2 input).
+//
+// Tile: 128 activation rows (one expert) x 128 weight rows, K streamed in
+// stages of 256 elements (one 128-byte swizzle row per operand row).
+// Warp roles (192 threads, one CTA per SM):
+//   warp 0     TMA producer: A and B code tiles (tiled TMA, 128B swizzle) and
+//              their scale atoms (bulk copies) into a 6-stage ring
+//   warp 1     TMEM owner; one lane issues tcgen05.cp (scales -> TMEM) and
+//              tcgen05.mma kind::mxf4nvf4.block_scale (M=128, N=128, K=64)
+//   warps 2-5  epilogue: tcgen05.ld of the f32 accumulator (double-buffered in
+//              TMEM so it overlaps the next tile's main loop), then either
+//              BF16 output (L2) or SwiGLU + NVFP4 requant (L1)
+// Tiles are ordered expert-major, then weight tile, then activation tile, so
+// the activation tiles sharing one weight tile run at the same time on
+// neighbouring SMs and the weight tile leaves HBM once.
+//
+// Every wait is bounded: a wait that exceeds the limit sets the device status
+// word, raises a shared abort flag that ends the other roles' loops, and the
+// CTA then waits (with a fixed bound) for its own copies and MMAs in flight,
+// frees its tensor memory and returns.
+#include "common.cuh"
+
+namespace nvfp4moe {
+
+__device__ int g_status[2];  // [0]: NVFP4MOE_OK or NVFP4MOE_ERR_DEVICE_TIMEOUT, [1]: wait site
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 128;
+constexpr int BK = 256;                       // K elements per stage
+constexpr int STAGES = 6;
+constexpr int kThreads = 192;
+constexpr int A_BYTES = BM * BK / 2;          // 16 KB
+constexpr int B_BYTES = BN * BK / 2;          // 16 KB
+constexpr int SF_BYTES = 4 * 512;             // 4 scale atoms (K=256) of 128 rows
+constexpr int OFF_B = STAGES * A_BYTES;
+constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
+constexpr int OFF_SFB = OFF_SFA + STAGES * SF_BYTES;
+constexpr int OFF_BAR = OFF_SFB + STAGES * SF_BYTES;
+constexpr int OFF_MISC = OFF_BAR + 256;
+constexpr int OFF_SCHED = OFF_MISC + 256;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t ACC_COLS = BN;             // f32 accumulator columns per buffer
+constexpr uint32_t SF_TMEM0 = 2 * ACC_COLS;   // scale slots start after 2 accumulators
+constexpr uint32_t SF_SLOT = 32;              // 16 columns SFA + 16 columns SFB per stage
+constexpr uint64_t kDrainLimitNs = 1000000000ull;
+
+static_assert(SF_TMEM0 + STAGES * SF_SLOT <= TMEM_COLS, "tensor memory budget");
+
+struct Params {
+  const uint8_t* a_sf;
+  const uint8_t* b_sf;
+  const float* gs_a;
+  const float* gs_b;
+  const int32_t* offsets;
+  int E;
+  int N;
+  int K;
+  int64_t sf_rowtile_bytes;   // (K/64) * 512: scale bytes of 128 rows
+  int64_t b_sf_expert_bytes;  // scale bytes of one expert's N x K weights
+  // plain epilogue
+  __nv_bfloat16* c;
+  int64_t ldc;
+  // SwiGLU epilogue
+  uint8_t* h_codes;
+  uint8_t* h_sf;
+  int64_t I;
+  const float* gs_h;
+  uint64_t wait_limit_ns;
+  int* status;
+};
+
+struct Sched {
+  const int32_t* tile_start;  // [E+1] first tile of each expert
+  const int32_t* pad_off;     // [E+1] padded first row of each expert
+  const int32_t* offsets;     // [E+1] compact first row of each expert
+  int E;
+  int NT;                     // weight tiles per expert
+  __device__ __forceinline__ void decode(int t, int& e, int& nb, int& mb, int& rows) const {
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {  // largest e with tile_start[e] <= t
+      const int mid = (lo + hi + 1) >> 1;
+      if (tile_start[mid] <= t) lo = mid;
+      else hi = mid - 1;
+    }
+    e = lo;
+    const int mt = (tile_start[e + 1] - tile_start[e]) / NT;
+    const int local = t - tile_start[e];
+    nb = local / mt;
+    mb = local - nb * mt;
+    const int cnt = offsets[e + 1] - offsets[e];
+    rows = min(BM, cnt - mb * BM);
+  }
+};
+
+// Bounded wait. Returns false on timeout (after raising the abort flag and
+// the device status) or when another role has aborted.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                             uint64_t limit_ns, int* status, int site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 15u) == 0) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > limit_ns) {
+        *abort_flag = 1;
+        if (atomicCAS(&status[0], 0, NVFP4MOE_ERR_DEVICE_TIMEOUT) == 0) status[1] = site;
+        return false;
+      }
+    }
+  }
+}
+
+// Wait used while shutting down: ignores the abort flag, fixed bound.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > kDrainLimitNs) return;
+  }
+}
+
+__device__ __forceinline__ void store_bf16x128(__nv_bfloat16* dst, const float* v, float alpha) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    uint32_t p[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat162 b = __floats2bfloat162_rn(v[8 * j + 2 * i] * alpha, v[8 * j + 2 * i + 1] * alpha);
+      p[i] = *reinterpret_cast<uint32_t*>(&b);
+    }
+    reinterpret_cast<uint4*>(dst)[j] = make_uint4(p[0], p[1], p[2], p[3]);
+  }
+}
+
+__device__ __forceinline__ float silu(float g) { return __fdiv_rn(g, 1.0f + expf(-g)); }
+
+template <bool kSwiGLU>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a16,
+                        const __grid_constant__ CUtensorMap tm_a32,
+                        const __grid_constant__ CUtensorMap tm_a64,
+                        const __grid_constant__ CUtensorMap tm_a128,
+                        const __grid_constant__ CUtensorMap tm_b, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t sbase = smem_addr(smem);
+  const uint32_t bar_full = sbase + OFF_BAR;               // STAGES x 8 bytes
+  const uint32_t bar_empty = bar_full + STAGES * 8;
+  const uint32_t bar_accf = bar_empty + STAGES * 8;        // 2 x 8 bytes
+  const uint32_t bar_acce = bar_accf + 16;
+  const uint32_t bar_aux = bar_acce + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+  int32_t* tile_start = reinterpret_cast<int32_t*>(smem + OFF_SCHED);
+  int32_t* pad_off = tile_start + (p.E + 1);
+  const int E = p.E, NT = p.N / BN;
+
+  // --- schedule: per expert its activation tiles (ceil(n_e/128)), prefix sums
+  if (warp == 0) {
+    int carry = 0;
+    for (int base = 0; base < E; base += 32) {
+      const int e = base + lane;
+      const int mt = e < E ? (p.offsets[e + 1] - p.offsets[e] + BM - 1) / BM : 0;
+      int incl = mt;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+        if (lane >= d) incl += y;
+      }
+      if (e < E) {
+        tile_start[e] = (carry + incl - mt) * NT;
+        pad_off[e] = (carry + incl - mt) * BM;
+      }
+      carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    }
+    if (lane == 0) {
+      tile_start[E] = carry * NT;
+      pad_off[E] = carry * BM;
+    }
+  }
+  if (tid == 32) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_accf + 8 * b, 1);
+      mbar_init(bar_acce + 8 * b, 4 * 32);
+    }
+    mbar_init(bar_aux, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int total = tile_start[E];
+  const Sched sch{tile_start, pad_off, p.offsets, E, NT};
+  const int ksteps = p.K / 64;
+  const int kblocks = (ksteps + 3) / 4;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------------------------------------------------------- producer
+    prefetch_tensormap(&tm_a16);
+    prefetch_tensormap(&tm_a32);
+    prefetch_tensormap(&tm_a64);
+    prefetch_tensormap(&tm_a128);
+    prefetch_tensormap(&tm_b);
+    const uint64_t pol_w = l2_policy_evict_first();  // weights: streamed once
+    const uint64_t pol_a = l2_policy_evict_last();   // activations: reused by every weight tile
+    uint32_t stage = 0, phase = 0, filled = 0, fill_phase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+      int e, nb, mb, rows;
+      sch.decode(t, e, nb, mb, rows);
+      const CUtensorMap* tma = rows <= 16 ? &tm_a16 : rows <= 32 ? &tm_a32 : rows <= 64 ? &tm_a64 : &tm_a128;
+      const int box = rows <= 16 ? 16 : rows <= 32 ? 32 : rows <= 64 ? 64 : 128;
+      const int a_row = pad_off[e] + mb * BM;
+      const int b_row = e * p.N + nb * BN;
+      const uint8_t* sfa = p.a_sf + (int64_t)(a_row / BM) * p.sf_rowtile_bytes;
+      const uint8_t* sfb = p.b_sf + (int64_t)e * p.b_sf_expert_bytes + (int64_t)(nb * BN / 128) * p.sf_rowtile_bytes;
+      for (int kb = 0; kb < kblocks; ++kb) {
+        const int nk = min(4, ksteps - kb * 4);
+        if (!wait_bounded(bar_empty + 8 * stage, phase ^ 1, abort_flag, p.wait_limit_ns, p.status, 1)) {
+          ok = false;
+          break;
+        }
+        const uint32_t full = bar_full + 8 * stage;
+        mbar_arrive_expect_tx(full, box * 128 + BN * 128 + 2 * nk * 512);
+        tma_load_2d(sbase + stage * A_BYTES, tma, full, kb * 128, a_row, pol_a);
+        tma_load_2d(sbase + OFF_B + stage * B_BYTES, &tm_b, full, kb * 128, b_row, pol_w);
+        bulk_load(sbase + OFF_SFA + stage * SF_BYTES, sfa + kb * 2048, nk * 512, full, pol_a);
+        bulk_load(sbase + OFF_SFB + stage * SF_BYTES, sfb + kb * 2048, nk * 512, full, pol_w);
+        filled |= 1u << stage;
+        fill_phase = (fill_phase & ~(1u << stage)) | (phase << stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+    // copies still in flight complete before the CTA may exit
+    if (!ok)
+      for (int s = 0; s < STAGES; ++s)
+        if ((filled >> s) & 1u) drain_wait(bar_full + 8 * s, (fill_phase >> s) & 1u);
+  } else if (warp == 1 && lane == 0) {
+    // ---------------------------------------------------------------- MMA issuer
+    const uint32_t idesc = idesc_nvf4(BM, BN);
+    uint32_t stage = 0, phase = 0, abuf = 0, aphase = 0;
+    bool ok = true, issued = false;
+    for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+      if (!wait_bounded(bar_acce + 8 * abuf, aphase ^ 1, abort_flag, p.wait_limit_ns, p.status, 2)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem + abuf * ACC_COLS;
+      for (int kb = 0; kb < kblocks; ++kb) {
+        const int nk = min(4, ksteps - kb * 4);
+        if (!wait_bounded(bar_full + 8 * stage, phase, abort_flag, p.wait_limit_ns, p.status, 3)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sfa_t = tmem + SF_TMEM0 + stage * SF_SLOT;
+        const uint32_t sfb_t = sfa_t + 16;
+        const uint32_t sa = sbase + stage * A_BYTES;
+        const uint32_t sb = sbase + OFF_B + stage * B_BYTES;
+        const uint32_t ssfa = sbase + OFF_SFA + stage * SF_BYTES;
+        const uint32_t ssfb = sbase + OFF_SFB + stage * SF_BYTES;
+        for (int kk = 0; kk < nk; ++kk) {
+          tc_cp_32x128b_warpx4(sfa_t + 4 * kk, sdesc_sf_atom(ssfa + kk * 512));
+          tc_cp_32x128b_warpx4(sfb_t + 4 * kk, sdesc_sf_atom(ssfb + kk * 512));
+        }
+        for (int kk = 0; kk < nk; ++kk)
+          tc_mma_nvf4(d_tmem, sdesc_kmajor_sw128(sa + kk * 32), sdesc_kmajor_sw128(sb + kk * 32), idesc,
+                      sfa_t + 4 * kk, sfb_t + 4 * kk, (kb | kk) != 0 ? 1u : 0u);
+        issued = true;
+        tc_commit(bar_empty + 8 * stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) break;
+      tc_commit(bar_accf + 8 * abuf);
+      if (++abuf == 2) {
+        abuf = 0;
+        aphase ^= 1;
+      }
+    }
+    if (!ok && issued) {
+      // tensor-core work in flight completes before the tensor memory is freed
+      tc_commit(bar_aux);
+      drain_wait(bar_aux, 0);
+    }
+  } else if (warp >= 2) {
+    // ---------------------------------------------------------------- epilogue
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    uint32_t abuf = 0, aphase = 0;
+    const float gs_a = *p.gs_a;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      int e, nb, mb, rows;
+      sch.decode(t, e, nb, mb, rows);
+      if (!wait_bounded(bar_accf + 8 * abuf, aphase, abort_flag, p.wait_limit_ns, p.status, 4)) break;
+      tc_fence_after();
+      float v[128];
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + abuf * ACC_COLS;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tc_ld32_wait(taddr + 32 * c, v + 32 * c);
+      tc_fence_before();
+      mbar_arrive(bar_acce + 8 * abuf);
+      if (++abuf == 2) {
+        abuf = 0;
+        aphase ^= 1;
+      }
+      if (row >= rows) continue;
+      const float alpha = 1.0f / (gs_a * p.gs_b[e]);
+      if constexpr (!kSwiGLU) {
+        const int64_t orow = (int64_t)p.offsets[e] + mb * BM + row;
+        store_bf16x128(p.c + orow * p.ldc + nb * BN, v, alpha);
+      } else {
+        // columns 32*b + [0,8) gate / [8,16) up of h features 16b..16b+7,
+        // columns 32*b + [16,24) gate / [24,32) up of h features 16b+8..16b+15
+        const float gs_h = *p.gs_h;
+        const int64_t hrow = (int64_t)pad_off[e] + mb * BM + row;
+        uint32_t words[8];
+        uint32_t sfw = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          float h[16];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            h[i] = silu(v[32 * b + i] * alpha) * (v[32 * b + 8 + i] * alpha);
+            h[8 + i] = silu(v[32 * b + 16 + i] * alpha) * (v[32 * b + 24 + i] * alpha);
+          }
+          const uint32_t sf = quantize_block16(h, gs_h, words[2 * b], words[2 * b + 1]);
+          sfw |= sf << (8 * b);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(p.h_codes + hrow * (p.I / 2) + nb * 32);
+        dst[0] = make_uint4(words[0], words[1], words[2], words[3]);
+        dst[1] = make_uint4(words[4], words[5], words[6], words[7]);
+        *reinterpret_cast<uint32_t*>(p.h_sf + sf_tiled_offset(hrow, nb * 4, p.I / 64)) = sfw;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// Rows of `row_bytes` bytes (K/2 codes), box of 128 bytes x box_rows rows,
+// 128-byte swizzle.
+bool make_codes_map(CUtensorMap* m, const void* base, int64_t rows, int64_t row_bytes, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int g_num_sms = 0;
+uint64_t g_wait_limit_ns = 4000000000ull;
+
+int num_sms() {
+  if (g_num_sms == 0) {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+      g_num_sms = n;
+  }
+  return g_num_sms;
+}
+
+size_t smem_bytes(int E) { return (size_t)OFF_SCHED + 8 * (size_t)(E + 1) + 1024; }
+
+template <bool kSwiGLU>
+int launch_grouped(const uint8_t* a_codes, int64_t a_rows, const uint8_t* b_codes, int N, int K,
+                   Params& p, cudaStream_t s) {
+  CUtensorMap ma[4], mb;
+  const int boxes[4] = {16, 32, 64, 128};
+  for (int i = 0; i < 4; ++i)
+    if (!make_codes_map(&ma[i], a_codes, a_rows, K / 2, boxes[i])) return NVFP4MOE_ERR_INVALID;
+  if (!make_codes_map(&mb, b_codes, (int64_t)p.E * N, K / 2, BN)) return NVFP4MOE_ERR_INVALID;
+  int* status = nullptr;
+  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_status) != cudaSuccess)
+    return NVFP4MOE_ERR_LAUNCH;
+  p.status = status;
+  p.wait_limit_ns = g_wait_limit_ns;
+  const size_t smem = smem_bytes(p.E);
+  auto kern = grouped_gemm_kernel<kSwiGLU>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return NVFP4MOE_ERR_LAUNCH;
+  const int grid = num_sms();
+  if (grid <= 0) return NVFP4MOE_ERR_LAUNCH;
+  kern<<<grid, kThreads, smem, s>>>(ma[0], ma[1], ma[2], ma[3], mb, p);
+  return launch_status();
+}
+
+int check_common(const uint8_t* a_codes, const uint8_t* a_sf, const float* gs_a, int64_t a_rows,
+                 const uint8_t* b_codes, const uint8_t* b_sf, const float* gs_b,
+                 const int32_t* offsets, int E, int64_t N, int64_t K) {
+  NVFP4_CHECK(E >= 1 && E <= 1024 && K > 0 && K % 64 == 0 && N > 0 && N % 128 == 0,
+              NVFP4MOE_ERR_UNSUPPORTED);
+  NVFP4_CHECK(K / 2 <= (1ll << 31) && (int64_t)E * N < (1ll << 31) && a_rows < (1ll << 31),
+              NVFP4MOE_ERR_UNSUPPORTED);
+  NVFP4_CHECK(a_codes && a_sf && gs_a && b_codes && b_sf && gs_b && offsets, NVFP4MOE_ERR_INVALID);
+  NVFP4_CHECK(aligned(a_codes, 16) && aligned(b_codes, 16) && aligned(a_sf, 16) && aligned(b_sf, 16),
+              NVFP4MOE_ERR_INVALID);
+  NVFP4_CHECK(a_rows >= 128 && a_rows % 128 == 0, NVFP4MOE_ERR_INVALID);
+  return NVFP4MOE_OK;
+}
+
+}  // namespace
+}  // namespace nvfp4moe
+
+using namespace nvfp4moe;
+
+extern "C" int nvfp4_grouped_gemm(const uint8_t* a_codes, const uint8_t* a_sf, const float* gs_a,
+                                  int64_t a_rows, const uint8_t* b_codes, const uint8_t* b_sf,
+                                  const float* gs_b, const int32_t* offsets, int E, int64_t N,
+                                  int64_t K, void* c, int64_t ldc, void* stream) {
+  NVFP4_TRY(check_common(a_codes, a_sf, gs_a, a_rows, b_codes, b_sf, gs_b, offsets, E, N, K));
+  NVFP4_CHECK(c && aligned(c, 16) && ldc >= N && ldc % 8 == 0, NVFP4MOE_ERR_INVALID);
+  Params p{};
+  p.a_sf = a_sf;
+  p.b_sf = b_sf;
+  p.gs_a = gs_a;
+  p.gs_b = gs_b;
+  p.offsets = offsets;
+  p.E = E;
+  p.N = (int)N;
+  p.K = (int)K;
+  p.sf_rowtile_bytes = (K / 64) * 512;
+  p.b_sf_expert_bytes = (int64_t)nvfp4_sf_bytes(N, K, NVFP4_SF_TILED);
+  p.c = static_cast<__nv_bfloat16*>(c);
+  p.ldc = ldc;
+  return launch_grouped<false>(a_codes, a_rows, b_codes, (int)N, (int)K, p, as_stream(stream));
+}
+
+extern "C" int nvfp4_grouped_gemm_swiglu(const uint8_t* a_codes, const uint8_t* a_sf,
+                                         const float* gs_a, int64_t a_rows, const uint8_t* w1_codes,
+                                         const uint8_t* w1_sf, const float* gs_w1,
+                                         const int32_t* offsets, int E, int64_t I, int64_t K,
+                                         const float* gs_h, uint8_t* h_codes, uint8_t* h_sf,
+                                         void* stream) {
+  NVFP4_CHECK(I > 0 && I % 64 == 0, NVFP4MOE_ERR_UNSUPPORTED);
+  NVFP4_TRY(check_common(a_codes, a_sf, gs_a, a_rows, w1_codes, w1_sf, gs_w1, offsets, E, 2 * I, K));
+  NVFP4_CHECK(gs_h && h_codes && h_sf && aligned(h_codes, 16) && aligned(h_sf, 16), NVFP4MOE_ERR_INVALID);
+  Params p{};
+  p.a_sf = a_sf;
+  p.b_sf = w1_sf;
+  p.gs_a = gs_a;
+  p.gs_b = gs_w1;
+  p.offsets = offsets;
+  p.E = E;
+  p.N = (int)(2 * I);
+  p.K = (int)K;
+  p.sf_rowtile_bytes = (K / 64) * 512;
+  p.b_sf_expert_bytes = (int64_t)nvfp4_sf_bytes(2 * I, K, NVFP4_SF_TILED);
+  p.h_codes = h_codes;
+  p.h_sf = h_sf;
+  p.I = I;
+  p.gs_h = gs_h;
+  return launch_grouped<true>(a_codes, a_rows, w1_codes, (int)(2 * I), (int)K, p, as_stream(stream));
+}
+
+extern "C" int nvfp4moe_last_device_status(void* stream) {
+  if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return NVFP4MOE_ERR_LAUNCH;
+  int host[2] = {0, 0};
+  if (cudaMemcpyFromSymbol(host, g_status, sizeof(host)) != cudaSuccess) return NVFP4MOE_ERR_LAUNCH;
+  const int zero[2] = {0, 0};
+  if (cudaMemcpyToSymbol(g_status, zero, sizeof(zero)) != cudaSuccess) return NVFP4MOE_ERR_LAUNCH;
+  return host[0];
+}
+
+extern "C" void nvfp4moe_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns = ns; }
+
+extern "C" int nvfp4moe_num_sms(void) { return num_sms(); }

@@ -1,0 +1,431 @@
+#!/usr/bin/env python3
+"""Benchmark of the NVFP4 MoE expert forward on GB300.
+
+One step = one moe_forward (route, permute, quantize, L1 grouped GEMM + SwiGLU
++ NVFP4 requant, L2 grouped GEMM, combine) over one batch of T tokens of a
+seeded synthetic workload, with weights and inputs resident in HBM. Prints one
+JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload prefill]
+  python bench.py --impl reference ...   # the CPU oracle on a bounded sample
+
+Multi-GPU: one process per GPU (torchrun); every rank runs an independent
+replica on its own tokens (the expert forward has no exchange step when the
+weights are replicated), the result is max-over-ranks time, "weak" scaling.
+"""
+import argparse
+import datetime
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer TFLOP/s & tokens/s at 1 GB300; % of FP4 tensor peak / HBM BW"
+FP4_OVER_BF16 = 13.5 / 2.25        # nominal dense FP4 / dense BF16 tensor rate
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNELS_PER_STEP = 10              # route 1, permute 3, quantize 3, L1 1, L2 1, combine 1
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="prefill",
+                    choices=["tiny", "decode", "prefill", "skewed", "prefill_small", "decode_small"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-experts", type=int, default=8,
+                    help="experts whose routed rows form the CPU-baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) of SM clock and throttle reasons."""
+
+    FIELDS = ["timestamp", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self, t_start=None, t_end=None):
+        """Summary of the samples taken between t_start and t_end (time.time())."""
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) != len(self.FIELDS):
+                    continue
+                try:
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                except ValueError:
+                    continue
+                if (t_start is None or ts >= t_start) and (t_end is None or ts <= t_end):
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        pw = [num(r[3]) for r in rows if num(r[3]) is not None]
+        load = sm
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(load or sm) if (load or sm) else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(rows), "samples_under_load": len(load)}
+
+
+# ---------------------------------------------------------------- helpers
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ["gemm.cu", "common.cuh"]:
+        with open(os.path.join(ROOT, "nvfp4_block_scaled_05_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload):
+    """dram bytes per launch of the L1 kernel from the committed ncu summary,
+    or None when the summary was taken on other kernel sources."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src = kernel_source_hash()
+    with open(path) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            kv = dict(p.split("=", 1) for p in line.split() if "=" in p)
+            if kv.get("workload") == workload and kv.get("kernel") == "l1_swiglu" and \
+                    kv.get("source") == src:
+                return float(kv["dram_bytes_per_launch"])
+    return None
+
+
+def layer_numbers(cfg, offsets):
+    """Algorithmic FLOPs and bytes of one forward and of the L1 kernel."""
+    counts = [offsets[e + 1] - offsets[e] for e in range(cfg.E)]
+    active = sum(1 for c in counts if c > 0)
+    K, I, M, T = cfg.K, cfg.I, cfg.M, cfg.T
+    w1 = 2 * I * (K // 2 + K // 16)
+    w2 = K * (I // 2 + I // 16)
+    flops = 6.0 * M * K * I
+    layer_bytes = active * (w1 + w2) + T * K * 2 * 2 + T * cfg.E * 4
+    l1_flops = 4.0 * M * K * I
+    l1_bytes = active * w1 + M * (K // 2 + K // 16) + M * (I // 2 + I // 16)
+    return dict(active=active, flops=flops, bytes=layer_bytes, l1_flops=l1_flops, l1_bytes=l1_bytes)
+
+
+# ---------------------------------------------------------------- oracle legs
+
+_HOST_INPUTS = {}
+
+
+def oracle_sample(cfg, seed, n_experts, step=0):
+    """Host inputs of a bounded sample: all routed rows of n_experts experts.
+    Inputs are drawn on the CPU (same distributions as the GPU workload)."""
+    import numpy as np
+    import oracle as O
+    from nvfp4_block_scaled_05_gb300 import workloads as W
+    key = (cfg.name, seed)
+    if key not in _HOST_INPUTS:
+        inp = W.moe_inputs(cfg, seed=seed, device="cpu", weights=False)
+        lg = inp["logits"].numpy()
+        _HOST_INPUTS[key] = (W.bf16_bits(inp["x"]), lg, O.route_topk(lg, cfg.k)[0])
+    x, logits, ids = _HOST_INPUTS[key]
+    counts = np.bincount(ids.ravel(), minlength=cfg.E)
+    active = [e for e in range(cfg.E) if counts[e] > 0]
+    experts = [active[(step * n_experts + i) % len(active)] for i in range(n_experts)]
+    qw = {}
+    for e in experts:
+        c1, s1, g1 = O.quantize_expert(W.bf16_bits(W.expert_weight(cfg, seed, 1, e)))
+        c2, s2, g2 = O.quantize_expert(W.bf16_bits(W.expert_weight(cfg, seed, 2, e)))
+        qw[e] = (c1, s1, g1, c2, s2, g2)
+    tokens = sorted(set(int(t) for t, j in zip(*np.nonzero(np.isin(ids, experts)))))
+    rows = int(np.isin(ids, experts).sum())
+    return dict(x=x, logits=logits, experts=experts, qw=qw, tokens=tokens, rows=rows)
+
+
+def time_oracle(cfg, sample):
+    import numpy as np
+    import oracle as O
+    t0 = time.perf_counter()
+    O.moe_forward(sample["x"], sample["logits"], None, None, cfg.k, np.float32(cfg.gs_h),
+                  tokens=sample["tokens"], experts=set(sample["experts"]),
+                  qweights=lambda e: sample["qw"][e])
+    dt = time.perf_counter() - t0
+    flops = 6.0 * cfg.K * cfg.I * sample["rows"]
+    return dt, flops
+
+
+def cpu_baseline(cfg, seed, n_experts):
+    import oracle as O
+    s = oracle_sample(cfg, seed, n_experts)
+    dt, flops = time_oracle(cfg, s)
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": O.get_threads(), "kind": "oracle",
+            "sample": "all %d routed rows of %d experts (%s) of the %s workload, routing and "
+                      "global scale over all %d tokens; weights quantized beforehand; %.1f s"
+                      % (s["rows"], n_experts, ",".join(map(str, s["experts"])), cfg.name, cfg.T, dt)}
+
+
+def run_reference(args, cfg):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle as O
+    n_exp = 1
+    samples = [oracle_sample(cfg, args.seed, n_exp, step=i) for i in range(args.warmup + args.steps)]
+    for s in samples[:args.warmup]:
+        time_oracle(cfg, s)
+    total_t, total_f, rows = 0.0, 0.0, 0
+    for s in samples[args.warmup:]:
+        dt, fl = time_oracle(cfg, s)
+        total_t += dt
+        total_f += fl
+        rows += s["rows"]
+    value = total_f / total_t / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": total_t / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
+            "config": {"workload": cfg.name, "T": cfg.T, "K": cfg.K, "I": cfg.I, "E": cfg.E, "k": cfg.k,
+                       "seed": args.seed, "step": "all routed rows of one expert per step"},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": O.get_threads(),
+                             "kind": "oracle",
+                             "sample": "%d steps x all routed rows of one expert (%d rows in total)"
+                                       % (args.steps, rows)},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU leg
+
+def run_ours(args, cfg):
+    import torch
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    from nvfp4_block_scaled_05_gb300 import binding as B
+    from nvfp4_block_scaled_05_gb300 import workloads as W
+
+    # inputs: replicated weights (same seed on every rank), per-rank tokens
+    inp = W.moe_inputs(cfg, seed=args.seed, device=dev, weights=True)
+    if rank:
+        tok = W.moe_inputs(cfg, seed=args.seed + 7919 * rank, device=dev, weights=False)
+        inp["x"], inp["logits"] = tok["x"], tok["logits"]
+    wts = B.prepare_moe_weights(inp["w1"], inp["w2"])
+    del inp["w1"], inp["w2"]
+    torch.cuda.empty_cache()
+    x, logits = inp["x"], inp["logits"]
+    gs_h = torch.tensor([cfg.gs_h], dtype=torch.float32, device=dev)
+    T, K, I, E, k = cfg.T, cfg.K, cfg.I, cfg.E, cfg.k
+    ws = torch.empty(B.moe_forward_workspace_size(T, K, I, E, k), dtype=torch.uint8, device=dev)
+    y = torch.empty((T, K), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        torch.cuda.synchronize()
+        if pg is not None:
+            pg.barrier()
+
+    # ---- device-resident timing of moe_forward
+    for _ in range(args.warmup):
+        B.moe_forward(x, logits, wts, k, gs_h, ws=ws, y=y)
+    st = B.nvfp4moe_last_device_status()
+    if st != 0:
+        raise RuntimeError("device status %d after warm-up" % st)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(1.0)                      # let the sampler start before the timed region
+    barrier()
+    t_start = time.time()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        B.moe_forward(x, logits, wts, k, gs_h, ws=ws, y=y)
+    ev1.record(stream)
+    barrier()
+    t_end = time.time()
+    clk = clocks.stop(t_start, t_end)
+    ms = ev0.elapsed_time(ev1) / args.steps
+    if B.nvfp4moe_last_device_status() != 0:
+        raise RuntimeError("device status after timed region")
+
+    # ---- per-stage device time (same stream, events between the six calls)
+    nst = len(B.STAGES)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(args.steps)]
+    barrier()
+    for i in range(args.steps):
+        B.moe_forward_stages(x, logits, wts, k, gs_h, ws, y, events=evs[i])
+    barrier()
+    stage_ms = {name: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)) / args.steps
+                for j, name in enumerate(B.STAGES)}
+
+    # ---- end to end through the public call, host buffers, copies timed
+    x_h = x.cpu().pin_memory()
+    l_h = logits.cpu().pin_memory()
+    y_h = torch.empty((T, K), dtype=torch.bfloat16).pin_memory()
+    x_d, l_d = torch.empty_like(x), torch.empty_like(logits)
+    for _ in range(max(1, args.warmup // 2)):
+        x_d.copy_(x_h, non_blocking=True)
+        l_d.copy_(l_h, non_blocking=True)
+        B.moe_forward(x_d, l_d, wts, k, gs_h, ws=ws, y=y)
+        y_h.copy_(y, non_blocking=True)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        x_d.copy_(x_h, non_blocking=True)
+        l_d.copy_(l_h, non_blocking=True)
+        B.moe_forward(x_d, l_d, wts, k, gs_h, ws=ws, y=y)
+        y_h.copy_(y, non_blocking=True)
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+
+    lay = B.moe_forward_workspace_layout(T, K, I, E, k)
+    offsets = ws[lay["offsets"]:lay["offsets"] + 4 * (E + 1)].view(torch.int32).cpu().tolist()
+    nums = layer_numbers(cfg, offsets)
+
+    if pg is not None:
+        t = torch.tensor([ms, e2e_ms, stage_ms["l1_swiglu"]], dtype=torch.float64, device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms, e2e_ms, l1_ms = t.tolist()
+    else:
+        l1_ms = stage_ms["l1_swiglu"]
+    if rank != 0:
+        if pg is not None:
+            pg.barrier()
+            pg.destroy_process_group()
+        return
+
+    peaks, peak_kind = load_peaks()
+    hbm_peak = float(peaks["hbm_gbs"])
+    fp4_peak = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])) * FP4_OVER_BF16
+    tflops = world * nums["flops"] / (ms * 1e-3) / 1e12
+    tokens_s = world * T / (ms * 1e-3)
+    # roofline of the dominant kernel (L1 grouped GEMM + SwiGLU + requant)
+    t_hbm = nums["l1_bytes"] / (hbm_peak * 1e9)
+    t_tc = nums["l1_flops"] / (fp4_peak * 1e12)
+    if t_hbm >= t_tc:
+        achieved = nums["l1_bytes"] / (l1_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                "frac": achieved / hbm_peak}
+    else:
+        achieved = nums["l1_flops"] / (l1_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": fp4_peak, "unit": "TFLOP/s",
+                "frac": achieved / fp4_peak}
+    roof["traffic"] = ncu_traffic(cfg.name)
+    roof["kernel"] = "l1_swiglu (grouped_gemm_kernel<true>)"
+    roof["kernel_ms"] = l1_ms
+    roof["peak_source"] = "%s (MEASURED_PEAKS.json)" % peak_kind if peak_kind == "measured" else "fallback"
+    if roof["bound"] == "tensor":
+        roof["peak_note"] = "measured sustained bf16 x 6 (nominal dense fp4/bf16 ratio)"
+    line = {
+        "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "nvfp4 (e2m1 x e4m3 block scale, f32 accumulate)",
+        "data": "synthetic (seeded; random-init weights of the layer shape)",
+        "config": {"workload": cfg.name, "T": T, "K": K, "I": I, "E": E, "k": k, "M": cfg.M,
+                   "global_tokens": world * T, "parallelism": "replicas x%d" % world,
+                   "active_experts": nums["active"], "seed": args.seed, "gs_h": cfg.gs_h,
+                   "l2": "inputs larger than L2: %.2f GB of expert weights streamed every step"
+                         % (nums["bytes"] / 1e9)},
+        "tokens_per_s": tokens_s,
+        "pct_fp4_peak": tflops / world / fp4_peak,
+        "pct_hbm_bw": nums["bytes"] / (ms * 1e-3) / 1e9 / hbm_peak,
+        "layer_bytes": nums["bytes"], "layer_flops": nums["flops"],
+        "stages_ms": stage_ms,
+        "roofline": roof,
+        "e2e": {"value": world * nums["flops"] / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": x.numel() * 2 + logits.numel() * 4,
+                "d2h_bytes_per_step": y.numel() * 2},
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "clocks": clk,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, args.seed, args.cpu_experts)
+    print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.barrier()
+        pg.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    from nvfp4_block_scaled_05_gb300 import workloads as W
+    cfg = W.CONFIGS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, cfg)
+    else:
+        run_ours(args, cfg)
+
+
+if __name__ == "__main__":
+    main()

@@ -294,3 +294,57 @@ def prepare_moe_weights(w1, w2, free_source=False):
         nvfp4_quantize(w2[e], codes=out["w2_codes"][e], sf=out["w2_sf"][e * sf2:(e + 1) * sf2],
                        gs_out=out["gs_w2"][e:e + 1])
     return out
+
+
+STAGES = ("route", "permute", "quantize", "l1_swiglu", "l2", "combine")
+
+
+def moe_forward_stages(x, logits, weights, k, gs_h, ws, y, events=None):
+    """The six C calls moe_forward makes, issued one by one on the current
+    stream with the same workspace carving, so that CUDA events can be
+    recorded between them: events, if given, is a list of len(STAGES) + 1
+    torch.cuda.Event; events[i] is recorded before stage i."""
+    T, K = x.shape
+    E = logits.shape[1]
+    I = weights["I"]
+    L = lib()
+    lay = moe_forward_workspace_layout(T, K, I, E, k)
+    base = ws.data_ptr()
+    p = {n: ctypes.c_void_p(base + o) for n, o in lay.items() if n != "a_rows"}
+    a_rows = lay["a_rows"]
+    M = T * k
+    up = lambda v: -(-v // 256) * 256
+    perm_ws = base + lay["out"] + up(M * K * 2)
+    perm_bytes = int(L.moe_permute_workspace_size(T, k, E))
+    disp_ws = perm_ws + up(perm_bytes)
+    disp_bytes = int(L.moe_quantize_dispatch_workspace_size(E))
+    s = _stream()
+    st = torch.cuda.current_stream()
+
+    def mark(i):
+        if events is not None:
+            events[i].record(st)
+
+    mark(0)
+    _check(L.moe_route_topk(_ptr(logits), T, E, k, p["topk_ids"], p["topk_w"], s), "route")
+    mark(1)
+    _check(L.moe_permute(p["topk_ids"], T, k, E, p["offsets"], p["perm_to_flat"], p["flat_to_perm"],
+                         ctypes.c_void_p(perm_ws), perm_bytes, s), "permute")
+    mark(2)
+    _check(L.moe_quantize_dispatch(_ptr(x), T, K, K, k, E, p["topk_ids"], p["offsets"], p["flat_to_perm"],
+                                   None, p["gs_x"], p["a_codes"], p["a_sf"], a_rows,
+                                   ctypes.c_void_p(disp_ws), disp_bytes, s), "quantize")
+    mark(3)
+    _check(L.nvfp4_grouped_gemm_swiglu(p["a_codes"], p["a_sf"], p["gs_x"], a_rows,
+                                       _ptr(weights["w1_codes"]), _ptr(weights["w1_sf"]),
+                                       _ptr(weights["gs_w1"]), p["offsets"], E, I, K, _ptr(gs_h),
+                                       p["h_codes"], p["h_sf"], s), "l1_swiglu")
+    mark(4)
+    _check(L.nvfp4_grouped_gemm(p["h_codes"], p["h_sf"], _ptr(gs_h), a_rows, _ptr(weights["w2_codes"]),
+                                _ptr(weights["w2_sf"]), _ptr(weights["gs_w2"]), p["offsets"], E, K, I,
+                                p["out"], K, s), "l2")
+    mark(5)
+    _check(L.moe_combine(p["out"], K, p["topk_w"], p["flat_to_perm"], T, k, K, _ptr(y), y.stride(0), s),
+           "combine")
+    mark(6)
+    return y

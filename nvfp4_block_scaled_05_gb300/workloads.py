@@ -77,6 +77,10 @@ CONFIGS = {
     "prefill": MoEConfig("prefill", T=8192, K=7168, I=2048, E=256, k=8, gs_h=28.0),
     "skewed": MoEConfig("skewed", T=16384, K=7168, I=2048, E=256, k=8, routing="zipf",
                         zipf_s=1.2, n_dead=16, gs_h=28.0),
+    # profiler-sized cases: the same layer and the same rows per expert as
+    # prefill / decode, with 32 experts (0.8 GB of weights, still above L2)
+    "prefill_small": MoEConfig("prefill_small", T=1024, K=7168, I=2048, E=32, k=8, gs_h=28.0),
+    "decode_small": MoEConfig("decode_small", T=16, K=7168, I=2048, E=32, k=8, gs_h=28.0),
 }
 
 # independent sub-streams of one seed
@@ -109,17 +113,22 @@ def moe_inputs(cfg: MoEConfig, seed: int = 0, device="cpu", weights=True):
     else:
         raise ValueError(cfg.routing)
     if weights:
-        out["w1"] = _randn((E, 2 * I, K), 0.02, seed, _W1, device, torch.bfloat16)
-        out["w2"] = _randn((E, K, I), 0.02, seed, _W2, device, torch.bfloat16)
+        out["w1"] = torch.empty((E, 2 * I, K), dtype=torch.bfloat16, device=device)
+        out["w2"] = torch.empty((E, K, I), dtype=torch.bfloat16, device=device)
+        for e in range(E):
+            out["w1"][e] = expert_weight(cfg, seed, 1, e, device)
+            out["w2"][e] = expert_weight(cfg, seed, 2, e, device)
     out["gs_h"] = float(cfg.gs_h)
     return out
 
 
-def expert_weights(cfg: MoEConfig, seed: int, device, which: int):
-    """Only W1 (which=1) or W2 (which=2); same values as moe_inputs()."""
-    if which == 1:
-        return _randn((cfg.E, 2 * cfg.I, cfg.K), 0.02, seed, _W1, device, torch.bfloat16)
-    return _randn((cfg.E, cfg.K, cfg.I), 0.02, seed, _W2, device, torch.bfloat16)
+def expert_weight(cfg: MoEConfig, seed: int, which: int, e: int, device="cpu"):
+    """W1[e] (which=1, shape (2I, K)) or W2[e] (which=2, shape (K, I)), drawn
+    from a generator of its own so one expert can be drawn alone; the values
+    equal moe_inputs()'s on the same device type."""
+    shape = (2 * cfg.I, cfg.K) if which == 1 else (cfg.K, cfg.I)
+    stream = (_W1 if which == 1 else _W2) * 100003 + e + 1
+    return _randn(shape, 0.02, seed, stream, device, torch.bfloat16)
 
 
 def _zipf_logits(cfg: MoEConfig, seed: int, device):

@@ -253,7 +253,8 @@ def quantize_expert(w_bf16: np.ndarray):
     return codes, sf, gs
 
 
-def moe_forward(x, logits, get_w1, get_w2, k, gs_h, tokens=None, keep=False):
+def moe_forward(x, logits, get_w1, get_w2, k, gs_h, tokens=None, keep=False, experts=None,
+                qweights=None):
     """README "MoE Runner", steps 1-6, for the tokens listed in ``tokens``.
 
     x: (T, K) BF16 bits; logits: (T, E) f32; get_w1(e) -> (2I, K) BF16 bits with
@@ -263,9 +264,12 @@ def moe_forward(x, logits, get_w1, get_w2, k, gs_h, tokens=None, keep=False):
 
     Routing, permutation and gs_x always cover all T tokens; the expert work is
     done for the listed tokens only, one expert at a time (so only one expert's
-    dequantized weights are held in memory). Returns a dict with the routing,
-    the permutation, gs_x, y (len(tokens), K) fp64, and per-(token, j)
-    intermediates when ``keep`` is set.
+    dequantized weights are held in memory). ``experts`` (optional) restricts
+    the expert work to the routed rows of those experts, so y then holds only
+    their share of the weighted sum. ``qweights`` (optional) maps an expert to
+    its already-quantized (c1, s1, g1, c2, s2, g2), skipping the offline weight
+    quantization. Returns a dict with the routing, the permutation, gs_x,
+    y (len(tokens), K) fp64, and per-(token, j) intermediates when ``keep``.
     """
     T, K = x.shape
     E = logits.shape[1]
@@ -279,13 +283,17 @@ def moe_forward(x, logits, get_w1, get_w2, k, gs_h, tokens=None, keep=False):
     by_expert = {}
     for ti, t in enumerate(tokens):
         for j in range(k):
-            by_expert.setdefault(int(ids[t, j]), []).append((ti, j))
+            if experts is None or int(ids[t, j]) in experts:
+                by_expert.setdefault(int(ids[t, j]), []).append((ti, j))
     outs = np.zeros((len(tokens), k, K), np.float64)
     inter = {}
     gs_w = {}
     for e in sorted(by_expert):
-        c1, s1, g1 = quantize_expert(get_w1(e))
-        c2, s2, g2 = quantize_expert(get_w2(e))
+        if qweights is not None:
+            c1, s1, g1, c2, s2, g2 = qweights(e)
+        else:
+            c1, s1, g1 = quantize_expert(get_w1(e))
+            c2, s2, g2 = quantize_expert(get_w2(e))
         gs_w[e] = (g1, g2)
         pairs = by_expert[e]
         a = xd[[ti for ti, _ in pairs]]

@@ -5,24 +5,31 @@
 // epilogue, extended with "Remaining Steps" 2-4: NVFP4 requantization in the
 // epilogue, FP4 codes and scales stored straight into the padded L2 input).
 //
-// Tile: 128 activation rows (one expert) x 128 weight rows, K streamed in
+// Tile: 128 activation rows (one expert) x 256 weight rows, one
+// tcgen05.mma kind::mxf4nvf4 (M=128, N=256, K=64) per 64 K; K streamed in
 // stages of 256 elements (one 128-byte swizzle row per operand row).
-// Warp roles (192 threads, one CTA per SM):
-//   warp 0     TMA producer: A and B code tiles (tiled TMA, 128B swizzle) and
-//              their scale atoms (bulk copies) into a 6-stage ring
-//   warp 1     TMEM owner; one lane issues tcgen05.cp (scales -> TMEM) and
-//              tcgen05.mma kind::mxf4nvf4.block_scale (M=128, N=128, K=64)
-//   warps 2-5  epilogue: tcgen05.ld of the f32 accumulator (double-buffered in
-//              TMEM so it overlaps the next tile's main loop), then either
-//              BF16 output (L2) or SwiGLU + NVFP4 requant (L1)
+// Measured on this part: an M=128 MMA costs the same issue time for N=64..256,
+// so N=256 is the shape that reaches the tensor-core rate; the scale-factor
+// copies into tensor memory (tcgen05.cp) cost about half an MMA each and run
+// concurrently with the MMAs only when a different warp issues them.
+// Warp roles (352 threads, one CTA per SM):
+//   warp 0      TMA producer: A and B code tiles (tiled TMA, 128B swizzle) and
+//               their scale atoms (bulk copies) into a 4-stage ring
+//   warp 1      TMEM owner; one lane issues the MMAs
+//   warp 2      one lane copies each stage's scale atoms into TMEM
+//               (tcgen05.cp 32x128b.warpx4), ahead of the MMAs
+//   warps 3-10  epilogue, two warps per TMEM lane quadrant (128 columns
+//               each): the f32 accumulator is moved to registers and released
+//               at once, so the next tile's MMAs overlap the epilogue math;
+//               then BF16 output (L2) or SwiGLU + NVFP4 requant (L1)
 // Tiles are ordered expert-major, then weight tile, then activation tile, so
 // the activation tiles sharing one weight tile run at the same time on
 // neighbouring SMs and the weight tile leaves HBM once.
 //
 // Every wait is bounded: a wait that exceeds the limit sets the device status
 // word, raises a shared abort flag that ends the other roles' loops, and the
-// CTA then waits (with a fixed bound) for its own copies and MMAs in flight,
-// frees its tensor memory and returns.
+// CTA then waits (with a fixed bound) for its own copies and tensor-core work
+// in flight, frees its tensor memory and returns.
 #include "common.cuh"
 
 namespace nvfp4moe {
@@ -32,26 +39,30 @@ __device__ int g_status[2];  // [0]: NVFP4MOE_OK or NVFP4MOE_ERR_DEVICE_TIMEOUT,
 namespace {
 
 constexpr int BM = 128;
-constexpr int BN = 128;
+constexpr int BN = 256;
 constexpr int BK = 256;                       // K elements per stage
-constexpr int STAGES = 6;
-constexpr int kThreads = 192;
+constexpr int STAGES = 4;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 32 * (3 + kEpiWarps);
 constexpr int A_BYTES = BM * BK / 2;          // 16 KB
-constexpr int B_BYTES = BN * BK / 2;          // 16 KB
-constexpr int SF_BYTES = 4 * 512;             // 4 scale atoms (K=256) of 128 rows
+constexpr int B_BYTES = BN * BK / 2;          // 32 KB
+constexpr int SFA_BYTES = 4 * 512;            // 4 scale atoms (K=256) of 128 rows
+constexpr int SFB_BYTES = 2 * SFA_BYTES;      // two 128-row halves of B
 constexpr int OFF_B = STAGES * A_BYTES;
 constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
-constexpr int OFF_SFB = OFF_SFA + STAGES * SF_BYTES;
-constexpr int OFF_BAR = OFF_SFB + STAGES * SF_BYTES;
+constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
+constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
 constexpr int OFF_MISC = OFF_BAR + 256;
 constexpr int OFF_SCHED = OFF_MISC + 256;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t ACC_COLS = BN;             // f32 accumulator columns per buffer
-constexpr uint32_t SF_TMEM0 = 2 * ACC_COLS;   // scale slots start after 2 accumulators
-constexpr uint32_t SF_SLOT = 32;              // 16 columns SFA + 16 columns SFB per stage
+constexpr uint32_t ACC_COLS = BN;             // one f32 accumulator of 256 columns
+constexpr uint32_t SF_TMEM0 = ACC_COLS;       // scale slots after the accumulator
+constexpr uint32_t SFA_COLS = 16;             // 4 k-steps x 4 columns
+constexpr uint32_t SF_SLOT = 48;              // 16 columns SFA + 32 columns SFB per stage
 constexpr uint64_t kDrainLimitNs = 1000000000ull;
 
 static_assert(SF_TMEM0 + STAGES * SF_SLOT <= TMEM_COLS, "tensor memory budget");
+static_assert(OFF_SCHED + 8 * 1025 + 1024 <= 232448, "shared memory budget");
 
 struct Params {
   const uint8_t* a_sf;
@@ -82,7 +93,8 @@ struct Sched {
   const int32_t* offsets;     // [E+1] compact first row of each expert
   int E;
   int NT;                     // weight tiles per expert
-  __device__ __forceinline__ void decode(int t, int& e, int& nb, int& mb, int& rows) const {
+  int N;
+  __device__ __forceinline__ void decode(int t, int& e, int& nb, int& mb, int& rows, int& ncols) const {
     int lo = 0, hi = E - 1;
     while (lo < hi) {  // largest e with tile_start[e] <= t
       const int mid = (lo + hi + 1) >> 1;
@@ -96,6 +108,7 @@ struct Sched {
     mb = local - nb * mt;
     const int cnt = offsets[e + 1] - offsets[e];
     rows = min(BM, cnt - mb * BM);
+    ncols = min(BN, N - nb * BN);   // 256, or 128 for the last tile when N % 256 == 128
   }
 };
 
@@ -129,17 +142,19 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 __device__ __forceinline__ void store_bf16x128(__nv_bfloat16* dst, const float* v, float alpha) {
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
-    uint32_t p[4];
+    uint32_t q[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       __nv_bfloat162 b = __floats2bfloat162_rn(v[8 * j + 2 * i] * alpha, v[8 * j + 2 * i + 1] * alpha);
-      p[i] = *reinterpret_cast<uint32_t*>(&b);
+      q[i] = *reinterpret_cast<uint32_t*>(&b);
     }
-    reinterpret_cast<uint4*>(dst)[j] = make_uint4(p[0], p[1], p[2], p[3]);
+    reinterpret_cast<uint4*>(dst)[j] = make_uint4(q[0], q[1], q[2], q[3]);
   }
 }
 
-__device__ __forceinline__ float silu(float g) { return __fdiv_rn(g, 1.0f + expf(-g)); }
+// silu(g) = g / (1 + exp(-g)) with the hardware exponential and reciprocal
+// (a few ulp; h is requantized to 4 bits right after).
+__device__ __forceinline__ float silu(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 template <bool kSwiGLU>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -153,16 +168,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t sbase = smem_addr(smem);
-  const uint32_t bar_full = sbase + OFF_BAR;               // STAGES x 8 bytes
-  const uint32_t bar_empty = bar_full + STAGES * 8;
-  const uint32_t bar_accf = bar_empty + STAGES * 8;        // 2 x 8 bytes
-  const uint32_t bar_acce = bar_accf + 16;
-  const uint32_t bar_aux = bar_acce + 16;
+  const uint32_t bar_full = sbase + OFF_BAR;               // STAGES x 8 bytes each
+  const uint32_t bar_sfready = bar_full + STAGES * 8;
+  const uint32_t bar_empty = bar_sfready + STAGES * 8;
+  const uint32_t bar_accf = bar_empty + STAGES * 8;
+  const uint32_t bar_acce = bar_accf + 8;
+  const uint32_t bar_aux = bar_acce + 8;                   // MMA drain on abort
+  const uint32_t bar_aux2 = bar_aux + 8;                   // scale-copy drain on abort
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
   int32_t* tile_start = reinterpret_cast<int32_t*>(smem + OFF_SCHED);
   int32_t* pad_off = tile_start + (p.E + 1);
-  const int E = p.E, NT = p.N / BN;
+  const int E = p.E, NT = (p.N + BN - 1) / BN;
 
   // --- schedule: per expert its activation tiles (ceil(n_e/128)), prefix sums
   if (warp == 0) {
@@ -190,13 +207,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 32) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_sfready + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(bar_accf + 8 * b, 1);
-      mbar_init(bar_acce + 8 * b, 4 * 32);
-    }
+    mbar_init(bar_accf, 1);
+    mbar_init(bar_acce, kEpiWarps * 32);
     mbar_init(bar_aux, 1);
+    mbar_init(bar_aux2, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -209,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int total = tile_start[E];
-  const Sched sch{tile_start, pad_off, p.offsets, E, NT};
+  const Sched sch{tile_start, pad_off, p.offsets, E, NT, p.N};
   const int ksteps = p.K / 64;
   const int kblocks = (ksteps + 3) / 4;
 
@@ -225,14 +242,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t stage = 0, phase = 0, filled = 0, fill_phase = 0;
     bool ok = true;
     for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-      int e, nb, mb, rows;
-      sch.decode(t, e, nb, mb, rows);
+      int e, nb, mb, rows, ncols;
+      sch.decode(t, e, nb, mb, rows, ncols);
       const CUtensorMap* tma = rows <= 16 ? &tm_a16 : rows <= 32 ? &tm_a32 : rows <= 64 ? &tm_a64 : &tm_a128;
       const int box = rows <= 16 ? 16 : rows <= 32 ? 32 : rows <= 64 ? 64 : 128;
       const int a_row = pad_off[e] + mb * BM;
       const int b_row = e * p.N + nb * BN;
+      const int bhalves = ncols / 128;
       const uint8_t* sfa = p.a_sf + (int64_t)(a_row / BM) * p.sf_rowtile_bytes;
-      const uint8_t* sfb = p.b_sf + (int64_t)e * p.b_sf_expert_bytes + (int64_t)(nb * BN / 128) * p.sf_rowtile_bytes;
+      const uint8_t* sfb = p.b_sf + (int64_t)e * p.b_sf_expert_bytes + (int64_t)(nb * 2) * p.sf_rowtile_bytes;
       for (int kb = 0; kb < kblocks; ++kb) {
         const int nk = min(4, ksteps - kb * 4);
         if (!wait_bounded(bar_empty + 8 * stage, phase ^ 1, abort_flag, p.wait_limit_ns, p.status, 1)) {
@@ -240,11 +258,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         const uint32_t full = bar_full + 8 * stage;
-        mbar_arrive_expect_tx(full, box * 128 + BN * 128 + 2 * nk * 512);
+        // the B box always moves 256 rows; rows past this expert's last weight
+        // tile are never multiplied (N=128 MMA), rows past the tensor read zeros
+        mbar_arrive_expect_tx(full, box * 128 + BN * 128 + (1 + bhalves) * nk * 512);
         tma_load_2d(sbase + stage * A_BYTES, tma, full, kb * 128, a_row, pol_a);
         tma_load_2d(sbase + OFF_B + stage * B_BYTES, &tm_b, full, kb * 128, b_row, pol_w);
-        bulk_load(sbase + OFF_SFA + stage * SF_BYTES, sfa + kb * 2048, nk * 512, full, pol_a);
-        bulk_load(sbase + OFF_SFB + stage * SF_BYTES, sfb + kb * 2048, nk * 512, full, pol_w);
+        bulk_load(sbase + OFF_SFA + stage * SFA_BYTES, sfa + kb * 2048, nk * 512, full, pol_a);
+        for (int h = 0; h < bhalves; ++h)
+          bulk_load(sbase + OFF_SFB + stage * SFB_BYTES + h * SFA_BYTES, sfb + h * p.sf_rowtile_bytes + kb * 2048,
+                    nk * 512, full, pol_w);
         filled |= 1u << stage;
         fill_phase = (fill_phase & ~(1u << stage)) | (phase << stage);
         if (++stage == STAGES) {
@@ -257,38 +279,69 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok)
       for (int s = 0; s < STAGES; ++s)
         if ((filled >> s) & 1u) drain_wait(bar_full + 8 * s, (fill_phase >> s) & 1u);
-  } else if (warp == 1 && lane == 0) {
-    // ---------------------------------------------------------------- MMA issuer
-    const uint32_t idesc = idesc_nvf4(BM, BN);
-    uint32_t stage = 0, phase = 0, abuf = 0, aphase = 0;
+  } else if (warp == 2 && lane == 0) {
+    // ---------------------------------------------------------------- scale copies
+    uint32_t stage = 0, phase = 0;
     bool ok = true, issued = false;
     for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-      if (!wait_bounded(bar_acce + 8 * abuf, aphase ^ 1, abort_flag, p.wait_limit_ns, p.status, 2)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t d_tmem = tmem + abuf * ACC_COLS;
+      int e, nb, mb, rows, ncols;
+      sch.decode(t, e, nb, mb, rows, ncols);
+      const int bhalves = ncols / 128;
       for (int kb = 0; kb < kblocks; ++kb) {
         const int nk = min(4, ksteps - kb * 4);
-        if (!wait_bounded(bar_full + 8 * stage, phase, abort_flag, p.wait_limit_ns, p.status, 3)) {
+        if (!wait_bounded(bar_full + 8 * stage, phase, abort_flag, p.wait_limit_ns, p.status, 5)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t sfa_t = tmem + SF_TMEM0 + stage * SF_SLOT;
-        const uint32_t sfb_t = sfa_t + 16;
-        const uint32_t sa = sbase + stage * A_BYTES;
-        const uint32_t sb = sbase + OFF_B + stage * B_BYTES;
-        const uint32_t ssfa = sbase + OFF_SFA + stage * SF_BYTES;
-        const uint32_t ssfb = sbase + OFF_SFB + stage * SF_BYTES;
+        const uint32_t sfb_t = sfa_t + SFA_COLS;
+        const uint32_t ssfa = sbase + OFF_SFA + stage * SFA_BYTES;
+        const uint32_t ssfb = sbase + OFF_SFB + stage * SFB_BYTES;
         for (int kk = 0; kk < nk; ++kk) {
           tc_cp_32x128b_warpx4(sfa_t + 4 * kk, sdesc_sf_atom(ssfa + kk * 512));
-          tc_cp_32x128b_warpx4(sfb_t + 4 * kk, sdesc_sf_atom(ssfb + kk * 512));
+          for (int h = 0; h < bhalves; ++h)
+            tc_cp_32x128b_warpx4(sfb_t + 8 * kk + 4 * h, sdesc_sf_atom(ssfb + h * SFA_BYTES + kk * 512));
         }
+        issued = true;
+        tc_commit(bar_sfready + 8 * stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+    if (!ok && issued) {
+      tc_commit(bar_aux2);
+      drain_wait(bar_aux2, 0);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------------------------------------------------------- MMA issuer
+    uint32_t stage = 0, phase = 0, aphase = 0;
+    bool ok = true, issued = false;
+    for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+      int e, nb, mb, rows, ncols;
+      sch.decode(t, e, nb, mb, rows, ncols);
+      const uint32_t idesc = idesc_nvf4(BM, ncols);
+      if (!wait_bounded(bar_acce, aphase ^ 1, abort_flag, p.wait_limit_ns, p.status, 2)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      for (int kb = 0; kb < kblocks; ++kb) {
+        const int nk = min(4, ksteps - kb * 4);
+        if (!wait_bounded(bar_sfready + 8 * stage, phase, abort_flag, p.wait_limit_ns, p.status, 3)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sfa_t = tmem + SF_TMEM0 + stage * SF_SLOT;
+        const uint32_t sfb_t = sfa_t + SFA_COLS;
+        const uint32_t sa = sbase + stage * A_BYTES;
+        const uint32_t sb = sbase + OFF_B + stage * B_BYTES;
         for (int kk = 0; kk < nk; ++kk)
-          tc_mma_nvf4(d_tmem, sdesc_kmajor_sw128(sa + kk * 32), sdesc_kmajor_sw128(sb + kk * 32), idesc,
-                      sfa_t + 4 * kk, sfb_t + 4 * kk, (kb | kk) != 0 ? 1u : 0u);
+          tc_mma_nvf4(tmem, sdesc_kmajor_sw128(sa + kk * 32), sdesc_kmajor_sw128(sb + kk * 32), idesc,
+                      sfa_t + 4 * kk, sfb_t + 8 * kk, (kb | kk) != 0 ? 1u : 0u);
         issued = true;
         tc_commit(bar_empty + 8 * stage);
         if (++stage == STAGES) {
@@ -297,48 +350,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
-      tc_commit(bar_accf + 8 * abuf);
-      if (++abuf == 2) {
-        abuf = 0;
-        aphase ^= 1;
-      }
+      tc_commit(bar_accf);
+      aphase ^= 1;
     }
     if (!ok && issued) {
       // tensor-core work in flight completes before the tensor memory is freed
       tc_commit(bar_aux);
       drain_wait(bar_aux, 0);
     }
-  } else if (warp >= 2) {
+  } else if (warp >= 3) {
     // ---------------------------------------------------------------- epilogue
-    const int quad = warp & 3;
+    const int quad = warp & 3;                 // TMEM lane quadrant this warp may access
+    const int half = (warp - 3) >> 2;          // columns [128*half, 128*half + 128)
     const int row = quad * 32 + lane;
-    uint32_t abuf = 0, aphase = 0;
+    uint32_t aphase = 0;
     const float gs_a = *p.gs_a;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      int e, nb, mb, rows;
-      sch.decode(t, e, nb, mb, rows);
-      if (!wait_bounded(bar_accf + 8 * abuf, aphase, abort_flag, p.wait_limit_ns, p.status, 4)) break;
+      int e, nb, mb, rows, ncols;
+      sch.decode(t, e, nb, mb, rows, ncols);
+      if (!wait_bounded(bar_accf, aphase, abort_flag, p.wait_limit_ns, p.status, 4)) break;
+      aphase ^= 1;
       tc_fence_after();
       float v[128];
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + abuf * ACC_COLS;
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + half * 128;
 #pragma unroll
       for (int c = 0; c < 4; ++c) tc_ld32_wait(taddr + 32 * c, v + 32 * c);
       tc_fence_before();
-      mbar_arrive(bar_acce + 8 * abuf);
-      if (++abuf == 2) {
-        abuf = 0;
-        aphase ^= 1;
-      }
-      if (row >= rows) continue;
+      mbar_arrive(bar_acce);
+      if (row >= rows || half * 128 >= ncols) continue;
       const float alpha = 1.0f / (gs_a * p.gs_b[e]);
       if constexpr (!kSwiGLU) {
         const int64_t orow = (int64_t)p.offsets[e] + mb * BM + row;
-        store_bf16x128(p.c + orow * p.ldc + nb * BN, v, alpha);
+        store_bf16x128(p.c + orow * p.ldc + nb * BN + half * 128, v, alpha);
       } else {
         // columns 32*b + [0,8) gate / [8,16) up of h features 16b..16b+7,
         // columns 32*b + [16,24) gate / [24,32) up of h features 16b+8..16b+15
         const float gs_h = *p.gs_h;
         const int64_t hrow = (int64_t)pad_off[e] + mb * BM + row;
+        const int64_t hfeat = (int64_t)nb * (BN / 2) + half * 64;   // first h feature of this thread
         uint32_t words[8];
         uint32_t sfw = 0;
 #pragma unroll
@@ -352,10 +401,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sf = quantize_block16(h, gs_h, words[2 * b], words[2 * b + 1]);
           sfw |= sf << (8 * b);
         }
-        uint4* dst = reinterpret_cast<uint4*>(p.h_codes + hrow * (p.I / 2) + nb * 32);
+        uint4* dst = reinterpret_cast<uint4*>(p.h_codes + hrow * (p.I / 2) + hfeat / 2);
         dst[0] = make_uint4(words[0], words[1], words[2], words[3]);
         dst[1] = make_uint4(words[4], words[5], words[6], words[7]);
-        *reinterpret_cast<uint32_t*>(p.h_sf + sf_tiled_offset(hrow, nb * 4, p.I / 64)) = sfw;
+        *reinterpret_cast<uint32_t*>(p.h_sf + sf_tiled_offset(hrow, hfeat / 16, p.I / 64)) = sfw;
       }
     }
   }

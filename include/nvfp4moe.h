@@ -166,6 +166,28 @@ int moe_permute(const int32_t* topk_ids, int64_t T, int k, int E,
                 int32_t* offsets, int32_t* perm_to_flat, int32_t* flat_to_perm,
                 void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * moe_permute_static_ws -- moe_permute without a workspace argument. The
+ * pages have no counterpart: this entry point serves callers that cannot
+ * allocate device memory where they call it (for example inside another
+ * framework's execution callback that forbids allocation, or on a path that
+ * must not risk the device synchronisation an allocation can bring) and have
+ * no workspace to pass. Results are identical to moe_permute's.
+ *   Scratch: a fixed 1 MiB device array inside the library, which every GPU
+ *   that loads the library holds until the process exits. It must fit
+ *   ceil(T*k / 1024) * E int32 entries (<= 262144); larger requests return
+ *   NVFP4MOE_ERR_WORKSPACE before anything is launched.
+ *   The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   All calls share the one array: calls whose kernels may overlap on the GPU
+ *   (several streams, several host threads) race on it. Nothing in it has to
+ *   start at zero; each call overwrites what it reads.
+ *   The call itself allocates nothing.
+ */
+int moe_permute_static_ws(const int32_t* topk_ids, int64_t T, int k, int E,
+                          int32_t* offsets, int32_t* perm_to_flat, int32_t* flat_to_perm,
+                          void* stream);
+
 /* Workspace bytes moe_quantize_dispatch needs. */
 size_t moe_quantize_dispatch_workspace_size(int E);
 

@@ -33,6 +33,8 @@ _SIGS = {
     "moe_permute_workspace_size": (_size, [_i64, _int, _int]),
     "moe_permute": (_int, [_c_void_p, _i64, _int, _int, _c_void_p, _c_void_p, _c_void_p,
                            _c_void_p, _size, _c_void_p]),
+    "moe_permute_static_ws": (_int, [_c_void_p, _i64, _int, _int, _c_void_p, _c_void_p, _c_void_p,
+                                     _c_void_p]),
     "moe_quantize_dispatch_workspace_size": (_size, [_int]),
     "moe_quantize_dispatch": (_int, [_c_void_p, _i64, _i64, _i64, _int, _int, _c_void_p,
                                      _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
@@ -187,6 +189,20 @@ def moe_permute(topk_ids, E):
     ws = torch.empty(max(nb, 1), dtype=torch.uint8, device=dev)
     _check(lib().moe_permute(_ptr(topk_ids), T, k, E, _ptr(offsets), _ptr(p2f), _ptr(f2p), _ptr(ws),
                              nb, _stream()), "moe_permute")
+    return offsets, p2f, f2p
+
+
+def moe_permute_static_ws(topk_ids, E):
+    """moe_permute using the library's fixed scratch array: no workspace is
+    allocated or passed (for callers that cannot allocate at the call)."""
+    _dev(topk_ids, "topk_ids")
+    T, k = topk_ids.shape
+    dev = topk_ids.device
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    p2f = torch.empty(T * k, dtype=torch.int32, device=dev)
+    f2p = torch.empty(T * k, dtype=torch.int32, device=dev)
+    _check(lib().moe_permute_static_ws(_ptr(topk_ids), T, k, E, _ptr(offsets), _ptr(p2f), _ptr(f2p),
+                                       _stream()), "moe_permute_static_ws")
     return offsets, p2f, f2p
 
 

@@ -13,6 +13,8 @@
 //               the rank among lower lanes gives the stable position.
 #include "common.cuh"
 
+#include <mutex>
+
 namespace nvfp4moe {
 namespace {
 
@@ -256,5 +258,69 @@ extern "C" int moe_combine(const void* out, int64_t ldo, const float* topk_w,
   combine_kernel<<<(unsigned)T, 128, 0, as_stream(stream)>>>(
       static_cast<const __nv_bfloat16*>(out), ldo, topk_w, flat_to_perm, k, K,
       static_cast<__nv_bfloat16*>(y), ldy);
+  return launch_status();
+}
+
+// ------------------------------------------------------------------ permutation without workspace
+//
+// moe_permute_static_ws: the same three kernels as moe_permute, with their
+// per-chunk count table in a fixed device array that the library owns,
+// instead of in caller-provided workspace. It exists for callers that cannot
+// allocate device memory at the point of the call -- for example code that
+// runs inside another framework's execution callback whose contract forbids
+// allocation, or latency-critical paths that must not risk the implicit
+// device synchronisation an allocation can cause -- and that have no spare
+// workspace to hand in.
+
+namespace {
+
+// ceil(T*k / 1024) * E count entries: 1 MiB of int32. Every GPU that loads
+// this library keeps this array until the process exits.
+constexpr int64_t kStaticPermScratchInts = 262144;
+static __device__ __align__(256) int32_t g_static_perm_scratch[kStaticPermScratchInts];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_perm_mutex;
+int32_t* g_static_perm_addr[kMaxDevices] = {};
+
+// Device address of the array on the current device. In host code the array's
+// name only stands in for it, so the address is looked up (once per device,
+// with that device current) and handed to the kernels as an ordinary pointer.
+int32_t* static_perm_scratch() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_static_perm_mutex);
+  if (!g_static_perm_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_perm_scratch) != cudaSuccess) return nullptr;
+    g_static_perm_addr[dev] = static_cast<int32_t*>(p);
+  }
+  return g_static_perm_addr[dev];
+}
+
+}  // namespace
+
+extern "C" int moe_permute_static_ws(const int32_t* topk_ids, int64_t T, int k, int E,
+                                     int32_t* offsets, int32_t* perm_to_flat,
+                                     int32_t* flat_to_perm, void* stream) {
+  NVFP4_CHECK(T >= 0 && k >= 1 && k <= 16 && E >= 1 && E <= 1024, NVFP4MOE_ERR_UNSUPPORTED);
+  NVFP4_CHECK(T * k < (1ll << 31), NVFP4MOE_ERR_UNSUPPORTED);
+  const int64_t n = T * k;
+  const int64_t nchunk = ceil_div(n, kPermChunk);
+  // the count table needs nchunk * E entries of the fixed array
+  NVFP4_CHECK(nchunk * E <= kStaticPermScratchInts, NVFP4MOE_ERR_WORKSPACE);
+  NVFP4_CHECK(offsets, NVFP4MOE_ERR_INVALID);
+  NVFP4_CHECK(n == 0 || (topk_ids && perm_to_flat && flat_to_perm), NVFP4MOE_ERR_INVALID);
+  int32_t* counts = static_perm_scratch();
+  NVFP4_CHECK(counts != nullptr, NVFP4MOE_ERR_LAUNCH);
+  cudaStream_t s = as_stream(stream);
+  // every entry the scan reads is written by the count kernel first, so the
+  // array needs no clearing between calls
+  if (nchunk > 0)
+    perm_count_kernel<<<(unsigned)nchunk, 256, E * sizeof(int32_t), s>>>(topk_ids, n, E, counts);
+  perm_scan_kernel<<<1, 1024, 0, s>>>(counts, (int)nchunk, E, n, offsets);
+  if (nchunk > 0)
+    perm_scatter_kernel<<<(unsigned)nchunk, 32, E * sizeof(int32_t), s>>>(topk_ids, n, E, counts,
+                                                                         perm_to_flat, flat_to_perm);
   return launch_status();
 }

@@ -65,6 +65,28 @@ def dist_env():
     return world, rank, local
 
 
+def rank_token_seed(seed, rank):
+    """Seed of the tokens (x, router logits) a rank processes: every rank runs
+    an independent replica of the layer on its own batch (same weights, seed
+    `seed`), so the work per rank is fixed as ranks are added (weak scaling)."""
+    return seed if rank == 0 else seed + 7919 * rank
+
+
+def max_over_ranks(values, pg, device):
+    """Elementwise maximum of per-rank timings (list of floats) over all ranks."""
+    import torch
+    if pg is None:
+        return list(values)
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return t.tolist()
+
+
+def aggregate_throughput(per_rank_flops, per_rank_tokens, world, ms):
+    """Whole-job TFLOP/s and tokens/s: all ranks' work over the slowest rank's time."""
+    return world * per_rank_flops / (ms * 1e-3) / 1e12, world * per_rank_tokens / (ms * 1e-3)
+
+
 # ---------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -277,7 +299,7 @@ def run_ours(args, cfg):
     # inputs: replicated weights (same seed on every rank), per-rank tokens
     inp = W.moe_inputs(cfg, seed=args.seed, device=dev, weights=True)
     if rank:
-        tok = W.moe_inputs(cfg, seed=args.seed + 7919 * rank, device=dev, weights=False)
+        tok = W.moe_inputs(cfg, seed=rank_token_seed(args.seed, rank), device=dev, weights=False)
         inp["x"], inp["logits"] = tok["x"], tok["logits"]
     wts = B.prepare_moe_weights(inp["w1"], inp["w2"])
     del inp["w1"], inp["w2"]
@@ -353,12 +375,7 @@ def run_ours(args, cfg):
     offsets = ws[lay["offsets"]:lay["offsets"] + 4 * (E + 1)].view(torch.int32).cpu().tolist()
     nums = layer_numbers(cfg, offsets)
 
-    if pg is not None:
-        t = torch.tensor([ms, e2e_ms, stage_ms["l1_swiglu"]], dtype=torch.float64, device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms, e2e_ms, l1_ms = t.tolist()
-    else:
-        l1_ms = stage_ms["l1_swiglu"]
+    ms, e2e_ms, l1_ms = max_over_ranks([ms, e2e_ms, stage_ms["l1_swiglu"]], pg, dev)
     if rank != 0:
         if pg is not None:
             pg.barrier()
@@ -368,8 +385,7 @@ def run_ours(args, cfg):
     peaks, peak_kind = load_peaks()
     hbm_peak = float(peaks["hbm_gbs"])
     fp4_peak = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])) * FP4_OVER_BF16
-    tflops = world * nums["flops"] / (ms * 1e-3) / 1e12
-    tokens_s = world * T / (ms * 1e-3)
+    tflops, tokens_s = aggregate_throughput(nums["flops"], T, world, ms)
     # roofline of the dominant kernel (L1 grouped GEMM + SwiGLU + requant)
     t_hbm = nums["l1_bytes"] / (hbm_peak * 1e9)
     t_tc = nums["l1_flops"] / (fp4_peak * 1e12)

@@ -1,0 +1,47 @@
+"""Failure detection without a GPU fault: every wait in the GEMM kernels is
+bounded. With the wait limit set to zero the waits run out, the kernel records
+NVFP4MOE_ERR_DEVICE_TIMEOUT in its status word, drains its own copies and
+tensor-core work, frees its tensor memory and returns; the host reads the
+status and the context stays usable for the next, normal launch."""
+import numpy as np
+import pytest
+import torch
+
+from nvfp4_block_scaled_05_gb300 import binding as B
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _operands():
+    g = torch.Generator().manual_seed(9)
+    E, K, N, per = 4, 1024, 256, 200
+    M = E * per
+    offsets = torch.arange(0, M + 1, per, dtype=torch.int32).to(DEV)
+    a_rows = B.nvfp4moe_padded_rows(M, E)
+    a_codes = torch.randint(0, 256, (a_rows, K // 2), dtype=torch.uint8, generator=g).to(DEV)
+    a_sf = torch.full((B.nvfp4_sf_bytes(a_rows, K),), 0x38, dtype=torch.uint8, device=DEV)
+    b_codes = torch.randint(0, 256, (E, N, K // 2), dtype=torch.uint8, generator=g).to(DEV)
+    b_sf = torch.full((E * B.nvfp4_sf_bytes(N, K),), 0x38, dtype=torch.uint8, device=DEV)
+    one = torch.ones(1, device=DEV)
+    gsb = torch.ones(E, device=DEV)
+    return a_codes, a_sf, one, b_codes, b_sf, gsb, offsets
+
+
+def test_wait_timeout_is_reported_and_context_survives():
+    ops = _operands()
+    assert B.nvfp4moe_last_device_status() == 0
+    good = B.nvfp4_grouped_gemm(*ops).clone()
+    assert B.nvfp4moe_last_device_status() == 0
+    try:
+        B.nvfp4moe_set_wait_limit_ns(0)
+        B.nvfp4_grouped_gemm(*ops)
+        st = B.nvfp4moe_last_device_status()
+    finally:
+        B.nvfp4moe_set_wait_limit_ns(4_000_000_000)
+    assert st == -5
+    # status was read and cleared; a normal launch still works and matches
+    again = B.nvfp4_grouped_gemm(*ops)
+    assert B.nvfp4moe_last_device_status() == 0
+    assert torch.equal(good, again)
+    assert torch.isfinite(good.float()).all()

@@ -299,6 +299,13 @@ int nvfp4moe_last_device_status(void* stream);
  * nanoseconds (default 4e9). Host only; affects launches made afterwards. */
 void nvfp4moe_set_wait_limit_ns(uint64_t ns);
 
+/* Test hook for the failure path: while set (non-zero), the MMA-issuing
+ * thread of every GEMM CTA that has work first waits on a barrier that
+ * nothing arrives on, so that bounded wait runs out after the wait limit and
+ * the kernel takes its abort path. Host only; affects launches made
+ * afterwards. */
+void nvfp4moe_set_test_stall(int on);
+
 /* Number of streaming multiprocessors of the current device (grid size of the
  * persistent GEMM kernels). Host only. */
 int nvfp4moe_num_sms(void);

@@ -54,6 +54,7 @@ _SIGS = {
                            _c_void_p, _c_void_p, _size, _c_void_p]),
     "nvfp4moe_last_device_status": (_int, [_c_void_p]),
     "nvfp4moe_set_wait_limit_ns": (None, [ctypes.c_uint64]),
+    "nvfp4moe_set_test_stall": (None, [_int]),
     "nvfp4moe_num_sms": (_int, []),
 }
 
@@ -126,6 +127,10 @@ def nvfp4moe_last_device_status():
 
 def nvfp4moe_set_wait_limit_ns(ns):
     lib().nvfp4moe_set_wait_limit_ns(int(ns))
+
+
+def nvfp4moe_set_test_stall(on):
+    lib().nvfp4moe_set_test_stall(1 if on else 0)
 
 
 def moe_forward_workspace_size(T, K, I, E, k):

@@ -85,6 +85,7 @@ struct Params {
   const float* gs_h;
   uint64_t wait_limit_ns;
   int* status;
+  int test_stall;             // test hook: the MMA issuer first waits on a barrier nobody arrives on
 };
 
 struct Sched {
@@ -175,6 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_acce = bar_accf + 8;
   const uint32_t bar_aux = bar_acce + 8;                   // MMA drain on abort
   const uint32_t bar_aux2 = bar_aux + 8;                   // scale-copy drain on abort
+  const uint32_t bar_never = bar_aux2 + 8;                 // never arrived on (failure-path test)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
   int32_t* tile_start = reinterpret_cast<int32_t*>(smem + OFF_SCHED);
@@ -214,6 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_acce, kEpiWarps * 32);
     mbar_init(bar_aux, 1);
     mbar_init(bar_aux2, 1);
+    mbar_init(bar_never, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -319,6 +322,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- MMA issuer
     uint32_t stage = 0, phase = 0, aphase = 0;
     bool ok = true, issued = false;
+    if (p.test_stall && blockIdx.x < total)
+      ok = wait_bounded(bar_never, 0, abort_flag, p.wait_limit_ns, p.status, 6);
     for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
       int e, nb, mb, rows, ncols;
       sch.decode(t, e, nb, mb, rows, ncols);
@@ -455,6 +460,7 @@ bool make_codes_map(CUtensorMap* m, const void* base, int64_t rows, int64_t row_
 
 int g_num_sms = 0;
 uint64_t g_wait_limit_ns = 4000000000ull;
+int g_test_stall = 0;
 
 int num_sms() {
   if (g_num_sms == 0) {
@@ -481,6 +487,7 @@ int launch_grouped(const uint8_t* a_codes, int64_t a_rows, const uint8_t* b_code
     return NVFP4MOE_ERR_LAUNCH;
   p.status = status;
   p.wait_limit_ns = g_wait_limit_ns;
+  p.test_stall = g_test_stall;
   const size_t smem = smem_bytes(p.E);
   auto kern = grouped_gemm_kernel<kSwiGLU>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
@@ -569,5 +576,7 @@ extern "C" int nvfp4moe_last_device_status(void* stream) {
 }
 
 extern "C" void nvfp4moe_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns = ns; }
+
+extern "C" void nvfp4moe_set_test_stall(int on) { g_test_stall = on ? 1 : 0; }
 
 extern "C" int nvfp4moe_num_sms(void) { return num_sms(); }

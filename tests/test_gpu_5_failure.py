@@ -1,8 +1,10 @@
 """Failure detection without a GPU fault: every wait in the GEMM kernels is
-bounded. With the wait limit set to zero the waits run out, the kernel records
-NVFP4MOE_ERR_DEVICE_TIMEOUT in its status word, drains its own copies and
-tensor-core work, frees its tensor memory and returns; the host reads the
-status and the context stays usable for the next, normal launch."""
+bounded. With the test stall on, the MMA-issuing thread waits on a barrier
+that nothing arrives on; after the (short) wait limit the kernel records
+NVFP4MOE_ERR_DEVICE_TIMEOUT in its status word, the other roles see the abort
+flag, drain their own copies and tensor-core work, free the tensor memory and
+return; the host reads the status and the context stays usable for the next,
+normal launch."""
 import numpy as np
 import pytest
 import torch
@@ -34,10 +36,12 @@ def test_wait_timeout_is_reported_and_context_survives():
     good = B.nvfp4_grouped_gemm(*ops).clone()
     assert B.nvfp4moe_last_device_status() == 0
     try:
-        B.nvfp4moe_set_wait_limit_ns(0)
+        B.nvfp4moe_set_wait_limit_ns(20_000_000)      # 20 ms
+        B.nvfp4moe_set_test_stall(True)
         B.nvfp4_grouped_gemm(*ops)
         st = B.nvfp4moe_last_device_status()
     finally:
+        B.nvfp4moe_set_test_stall(False)
         B.nvfp4moe_set_wait_limit_ns(4_000_000_000)
     assert st == -5
     # status was read and cleared; a normal launch still works and matches

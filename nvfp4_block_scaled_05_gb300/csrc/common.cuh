@@ -239,6 +239,20 @@ __device__ __forceinline__ void tc_mma_nvf4(uint32_t d, uint64_t adesc, uint64_t
       : "memory");
 }
 
+// Register -> TMEM stores of this warp's 32 lanes (its own lane quadrant):
+// one column, or eight consecutive columns.
+__device__ __forceinline__ void tc_st_x1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void tc_st_x8(uint32_t taddr, const uint4& a, const uint4& b) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+               "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // 32 consecutive f32 columns of this thread's TMEM lane, waited for.
 __device__ __forceinline__ void tc_ld32_wait(uint32_t taddr, float* out) {
   uint32_t r[32];

@@ -9,16 +9,21 @@
 // tcgen05.mma kind::mxf4nvf4 (M=128, N=256, K=64) per 64 K; K streamed in
 // stages of 256 elements (one 128-byte swizzle row per operand row).
 // Measured on this part: an M=128 MMA costs the same issue time for N=64..256,
-// so N=256 is the shape that reaches the tensor-core rate; the scale-factor
-// copies into tensor memory (tcgen05.cp) cost about half an MMA each and run
-// concurrently with the MMAs only when a different warp issues them.
-// Warp roles (352 threads, one CTA per SM):
+// so N=256 is the shape that reaches the tensor-core rate. The block scales
+// must sit in tensor memory before each MMA; moving them with tcgen05.cp
+// (about 35 bytes of TMEM per cycle, one copy engine) costs more than the MMAs
+// it feeds, so four warps write them with tcgen05.st instead, each into its
+// own TMEM lane quadrant, in parallel.
+// Warp roles (448 threads, one CTA per SM):
 //   warp 0      TMA producer: A and B code tiles (tiled TMA, 128B swizzle) and
 //               their scale atoms (bulk copies) into a 4-stage ring
 //   warp 1      TMEM owner; one lane issues the MMAs
-//   warp 2      one lane copies each stage's scale atoms into TMEM
-//               (tcgen05.cp 32x128b.warpx4), ahead of the MMAs
-//   warps 3-10  epilogue, two warps per TMEM lane quadrant (128 columns
+//   warps 2-5   scale warps, one per TMEM lane quadrant q: per K=64 step the A
+//               scale of each of the quadrant's 32 rows goes to column 4kk+q
+//               (the MMA reads quadrant q's A scales from column base+q), and
+//               the 256 B-row scales to columns 8kk..8kk+7 (B scales are read
+//               in every quadrant, so each quadrant holds its own copy)
+//   warps 6-13  epilogue, two warps per TMEM lane quadrant (128 columns
 //               each): the f32 accumulator is moved to registers and released
 //               at once, so the next tile's MMAs overlap the epilogue math;
 //               then BF16 output (L2) or SwiGLU + NVFP4 requant (L1)
@@ -42,8 +47,10 @@ constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 256;                       // K elements per stage
 constexpr int STAGES = 4;
+constexpr int kScaleWarps = 4;
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = 32 * (3 + kEpiWarps);
+constexpr int kFirstEpiWarp = 2 + kScaleWarps;
+constexpr int kThreads = 32 * (2 + kScaleWarps + kEpiWarps);
 constexpr int A_BYTES = BM * BK / 2;          // 16 KB
 constexpr int B_BYTES = BN * BK / 2;          // 32 KB
 constexpr int SFA_BYTES = 4 * 512;            // 4 scale atoms (K=256) of 128 rows
@@ -140,19 +147,6 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
-__device__ __forceinline__ void store_bf16x128(__nv_bfloat16* dst, const float* v, float alpha) {
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    uint32_t q[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      __nv_bfloat162 b = __floats2bfloat162_rn(v[8 * j + 2 * i] * alpha, v[8 * j + 2 * i + 1] * alpha);
-      q[i] = *reinterpret_cast<uint32_t*>(&b);
-    }
-    reinterpret_cast<uint4*>(dst)[j] = make_uint4(q[0], q[1], q[2], q[3]);
-  }
-}
-
 // silu(g) = g / (1 + exp(-g)) with the hardware exponential and reciprocal
 // (a few ulp; h is requantized to 4 bits right after).
 __device__ __forceinline__ float silu(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
@@ -175,8 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_accf = bar_empty + STAGES * 8;
   const uint32_t bar_acce = bar_accf + 8;
   const uint32_t bar_aux = bar_acce + 8;                   // MMA drain on abort
-  const uint32_t bar_aux2 = bar_aux + 8;                   // scale-copy drain on abort
-  const uint32_t bar_never = bar_aux2 + 8;                 // never arrived on (failure-path test)
+  const uint32_t bar_never = bar_aux + 8;                  // never arrived on (failure-path test)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
   int32_t* tile_start = reinterpret_cast<int32_t*>(smem + OFF_SCHED);
@@ -209,13 +202,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 32) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_sfready + 8 * s, 1);
+      mbar_init(bar_sfready + 8 * s, kScaleWarps);
       mbar_init(bar_empty + 8 * s, 1);
     }
     mbar_init(bar_accf, 1);
     mbar_init(bar_acce, kEpiWarps * 32);
     mbar_init(bar_aux, 1);
-    mbar_init(bar_aux2, 1);
     mbar_init(bar_never, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -282,41 +274,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok)
       for (int s = 0; s < STAGES; ++s)
         if ((filled >> s) & 1u) drain_wait(bar_full + 8 * s, (fill_phase >> s) & 1u);
-  } else if (warp == 2 && lane == 0) {
-    // ---------------------------------------------------------------- scale copies
+  } else if (warp >= 2 && warp < kFirstEpiWarp) {
+    // ---------------------------------------------------------------- scale warps
+    const int q = warp & 3;                               // TMEM lane quadrant of this warp
+    const uint32_t lanes = static_cast<uint32_t>(q * 32) << 16;
     uint32_t stage = 0, phase = 0;
-    bool ok = true, issued = false;
+    bool ok = true;
     for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-      int e, nb, mb, rows, ncols;
-      sch.decode(t, e, nb, mb, rows, ncols);
-      const int bhalves = ncols / 128;
       for (int kb = 0; kb < kblocks; ++kb) {
         const int nk = min(4, ksteps - kb * 4);
-        if (!wait_bounded(bar_full + 8 * stage, phase, abort_flag, p.wait_limit_ns, p.status, 5)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t sfa_t = tmem + SF_TMEM0 + stage * SF_SLOT;
+        // every lane waits, then the warp agrees (the stores below are warp-wide)
+        ok = wait_bounded(bar_full + 8 * stage, phase, abort_flag, p.wait_limit_ns, p.status, 5);
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        if (!ok) break;
+        const uint32_t sfa_t = tmem + lanes + SF_TMEM0 + stage * SF_SLOT;
         const uint32_t sfb_t = sfa_t + SFA_COLS;
-        const uint32_t ssfa = sbase + OFF_SFA + stage * SFA_BYTES;
-        const uint32_t ssfb = sbase + OFF_SFB + stage * SFB_BYTES;
+        const uint8_t* ssfa = smem + OFF_SFA + stage * SFA_BYTES + lane * 16;
+        const uint8_t* ssfb = smem + OFF_SFB + stage * SFB_BYTES + lane * 16;
         for (int kk = 0; kk < nk; ++kk) {
-          tc_cp_32x128b_warpx4(sfa_t + 4 * kk, sdesc_sf_atom(ssfa + kk * 512));
-          for (int h = 0; h < bhalves; ++h)
-            tc_cp_32x128b_warpx4(sfb_t + 8 * kk + 4 * h, sdesc_sf_atom(ssfb + h * SFA_BYTES + kk * 512));
+          // atom layout: chunk `lane` of a 512-byte atom holds rows lane, lane+32,
+          // lane+64, lane+96 (4 bytes each); the word of row 32q+lane is word q
+          const uint32_t a_sf = *reinterpret_cast<const uint32_t*>(ssfa + kk * 512 + q * 4);
+          // B rows lane+32j, j = 0..3 (first 128 rows) and 4..7 (second 128 rows);
+          // for a 128-column tile the second half is stale and never read
+          const uint4 b_lo = *reinterpret_cast<const uint4*>(ssfb + kk * 512);
+          const uint4 b_hi = *reinterpret_cast<const uint4*>(ssfb + SFA_BYTES + kk * 512);
+          tc_st_x1(sfa_t + 4 * kk + q, a_sf);
+          tc_st_x8(sfb_t + 8 * kk, b_lo, b_hi);
         }
-        issued = true;
-        tc_commit(bar_sfready + 8 * stage);
+        tc_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_sfready + 8 * stage);
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1;
         }
       }
-    }
-    if (!ok && issued) {
-      tc_commit(bar_aux2);
-      drain_wait(bar_aux2, 0);
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------------------- MMA issuer
@@ -363,10 +357,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_commit(bar_aux);
       drain_wait(bar_aux, 0);
     }
-  } else if (warp >= 3) {
+  } else if (warp >= kFirstEpiWarp) {
     // ---------------------------------------------------------------- epilogue
     const int quad = warp & 3;                 // TMEM lane quadrant this warp may access
-    const int half = (warp - 3) >> 2;          // columns [128*half, 128*half + 128)
+    const int half = (warp - kFirstEpiWarp) >> 2;   // columns [128*half, 128*half + 128)
     const int row = quad * 32 + lane;
     uint32_t aphase = 0;
     const float gs_a = *p.gs_a;
@@ -376,18 +370,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!wait_bounded(bar_accf, aphase, abort_flag, p.wait_limit_ns, p.status, 4)) break;
       aphase ^= 1;
       tc_fence_after();
-      float v[128];
       const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + half * 128;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tc_ld32_wait(taddr + 32 * c, v + 32 * c);
-      tc_fence_before();
-      mbar_arrive(bar_acce);
-      if (row >= rows || half * 128 >= ncols) continue;
-      const float alpha = 1.0f / (gs_a * p.gs_b[e]);
+      const bool active = row < rows && half * 128 < ncols;
+      const float alpha = active ? 1.0f / (gs_a * p.gs_b[e]) : 0.0f;
       if constexpr (!kSwiGLU) {
+        // BF16 output: each 32-column chunk is scaled and packed as it leaves
+        // TMEM (64 registers instead of 128), then the accumulator is released
+        uint32_t packed[64];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float v[32];
+          tc_ld32_wait(taddr + 32 * c, v);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * i] * alpha, v[2 * i + 1] * alpha);
+            packed[16 * c + i] = *reinterpret_cast<uint32_t*>(&b);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(bar_acce);
+        if (!active) continue;
         const int64_t orow = (int64_t)p.offsets[e] + mb * BM + row;
-        store_bf16x128(p.c + orow * p.ldc + nb * BN + half * 128, v, alpha);
+        uint4* dst = reinterpret_cast<uint4*>(p.c + orow * p.ldc + nb * BN + half * 128);
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          dst[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
       } else {
+        float v[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tc_ld32_wait(taddr + 32 * c, v + 32 * c);
+        tc_fence_before();
+        mbar_arrive(bar_acce);
+        if (!active) continue;
         // columns 32*b + [0,8) gate / [8,16) up of h features 16b..16b+7,
         // columns 32*b + [16,24) gate / [24,32) up of h features 16b+8..16b+15
         const float gs_h = *p.gs_h;

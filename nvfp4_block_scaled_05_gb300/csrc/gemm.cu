@@ -63,12 +63,17 @@ constexpr int OFF_MISC = OFF_BAR + 256;
 constexpr int OFF_SCHED = OFF_MISC + 256;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COLS = BN;             // one f32 accumulator of 256 columns
-constexpr uint32_t SF_TMEM0 = ACC_COLS;       // scale slots after the accumulator
-constexpr uint32_t SFA_COLS = 16;             // 4 k-steps x 4 columns
-constexpr uint32_t SF_SLOT = 48;              // 16 columns SFA + 32 columns SFB per stage
+// Scale slots after the accumulator. A TMEM store of n columns starts on a
+// multiple of n, so each stage's 32 SFB columns (k-step kk in columns 8kk ..
+// 8kk+7) start on a multiple of 32, and the SFA slots (quadrant q: k-step kk in
+// column 4kk + q, one-column stores) follow all of them.
+constexpr uint32_t SFB_TMEM0 = ACC_COLS;
+constexpr uint32_t SFB_SLOT = 32;
+constexpr uint32_t SFA_TMEM0 = SFB_TMEM0 + STAGES * SFB_SLOT;
+constexpr uint32_t SFA_SLOT = 16;
 constexpr uint64_t kDrainLimitNs = 1000000000ull;
 
-static_assert(SF_TMEM0 + STAGES * SF_SLOT <= TMEM_COLS, "tensor memory budget");
+static_assert(SFA_TMEM0 + STAGES * SFA_SLOT <= TMEM_COLS, "tensor memory budget");
 static_assert(OFF_SCHED + 8 * 1025 + 1024 <= 232448, "shared memory budget");
 
 struct Params {
@@ -170,6 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_acce = bar_accf + 8;
   const uint32_t bar_aux = bar_acce + 8;                   // MMA drain on abort
   const uint32_t bar_never = bar_aux + 8;                  // never arrived on (failure-path test)
+  const uint32_t bar_sffull = bar_never + 8;               // STAGES x 8 bytes: scale atoms landed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
   int32_t* tile_start = reinterpret_cast<int32_t*>(smem + OFF_SCHED);
@@ -202,6 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 32) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_sffull + 8 * s, 1);
       mbar_init(bar_sfready + 8 * s, kScaleWarps);
       mbar_init(bar_empty + 8 * s, 1);
     }
@@ -234,34 +241,53 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tensormap(&tm_b);
     const uint64_t pol_w = l2_policy_evict_first();  // weights: streamed once
     const uint64_t pol_a = l2_policy_evict_last();   // activations: reused by every weight tile
-    uint32_t stage = 0, phase = 0, filled = 0, fill_phase = 0;
-    bool ok = true;
-    for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+    // Copy sources of one tile, decoded one tile ahead of its loads.
+    struct TileSrc {
+      const CUtensorMap* tma;
+      int box, a_row, b_row, bhalves;
+      const uint8_t* sfa;
+      const uint8_t* sfb;
+    };
+    auto tile_src = [&](int t) {
       int e, nb, mb, rows, ncols;
       sch.decode(t, e, nb, mb, rows, ncols);
-      const CUtensorMap* tma = rows <= 16 ? &tm_a16 : rows <= 32 ? &tm_a32 : rows <= 64 ? &tm_a64 : &tm_a128;
-      const int box = rows <= 16 ? 16 : rows <= 32 ? 32 : rows <= 64 ? 64 : 128;
-      const int a_row = pad_off[e] + mb * BM;
-      const int b_row = e * p.N + nb * BN;
-      const int bhalves = ncols / 128;
-      const uint8_t* sfa = p.a_sf + (int64_t)(a_row / BM) * p.sf_rowtile_bytes;
-      const uint8_t* sfb = p.b_sf + (int64_t)e * p.b_sf_expert_bytes + (int64_t)(nb * 2) * p.sf_rowtile_bytes;
+      TileSrc c;
+      c.tma = rows <= 16 ? &tm_a16 : rows <= 32 ? &tm_a32 : rows <= 64 ? &tm_a64 : &tm_a128;
+      c.box = rows <= 16 ? 16 : rows <= 32 ? 32 : rows <= 64 ? 64 : 128;
+      c.a_row = pad_off[e] + mb * BM;
+      c.b_row = e * p.N + nb * BN;
+      c.bhalves = ncols / 128;
+      c.sfa = p.a_sf + (int64_t)(c.a_row / BM) * p.sf_rowtile_bytes;
+      c.sfb = p.b_sf + (int64_t)e * p.b_sf_expert_bytes + (int64_t)(nb * 2) * p.sf_rowtile_bytes;
+      return c;
+    };
+    uint32_t stage = 0, phase = 0, filled = 0, fill_phase = 0;
+    bool ok = true;
+    TileSrc cur{}, nxt{};
+    if (blockIdx.x < total) cur = tile_src(blockIdx.x);
+    for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+      const bool has_next = t + (int)gridDim.x < total;
+      if (has_next) nxt = tile_src(t + gridDim.x);
       for (int kb = 0; kb < kblocks; ++kb) {
         const int nk = min(4, ksteps - kb * 4);
         if (!wait_bounded(bar_empty + 8 * stage, phase ^ 1, abort_flag, p.wait_limit_ns, p.status, 1)) {
           ok = false;
           break;
         }
+        // codes and scales complete on separate barriers: the scale warps start
+        // as soon as the (small) scale atoms land
         const uint32_t full = bar_full + 8 * stage;
+        const uint32_t sffull = bar_sffull + 8 * stage;
+        mbar_arrive_expect_tx(sffull, (1 + cur.bhalves) * nk * 512);
+        bulk_load(sbase + OFF_SFA + stage * SFA_BYTES, cur.sfa + kb * 2048, nk * 512, sffull, pol_a);
+        for (int h = 0; h < cur.bhalves; ++h)
+          bulk_load(sbase + OFF_SFB + stage * SFB_BYTES + h * SFA_BYTES,
+                    cur.sfb + h * p.sf_rowtile_bytes + kb * 2048, nk * 512, sffull, pol_w);
         // the B box always moves 256 rows; rows past this expert's last weight
         // tile are never multiplied (N=128 MMA), rows past the tensor read zeros
-        mbar_arrive_expect_tx(full, box * 128 + BN * 128 + (1 + bhalves) * nk * 512);
-        tma_load_2d(sbase + stage * A_BYTES, tma, full, kb * 128, a_row, pol_a);
-        tma_load_2d(sbase + OFF_B + stage * B_BYTES, &tm_b, full, kb * 128, b_row, pol_w);
-        bulk_load(sbase + OFF_SFA + stage * SFA_BYTES, sfa + kb * 2048, nk * 512, full, pol_a);
-        for (int h = 0; h < bhalves; ++h)
-          bulk_load(sbase + OFF_SFB + stage * SFB_BYTES + h * SFA_BYTES, sfb + h * p.sf_rowtile_bytes + kb * 2048,
-                    nk * 512, full, pol_w);
+        mbar_arrive_expect_tx(full, cur.box * 128 + BN * 128);
+        tma_load_2d(sbase + stage * A_BYTES, cur.tma, full, kb * 128, cur.a_row, pol_a);
+        tma_load_2d(sbase + OFF_B + stage * B_BYTES, &tm_b, full, kb * 128, cur.b_row, pol_w);
         filled |= 1u << stage;
         fill_phase = (fill_phase & ~(1u << stage)) | (phase << stage);
         if (++stage == STAGES) {
@@ -269,11 +295,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           phase ^= 1;
         }
       }
+      cur = nxt;
     }
     // copies still in flight complete before the CTA may exit
     if (!ok)
       for (int s = 0; s < STAGES; ++s)
-        if ((filled >> s) & 1u) drain_wait(bar_full + 8 * s, (fill_phase >> s) & 1u);
+        if ((filled >> s) & 1u) {
+          drain_wait(bar_full + 8 * s, (fill_phase >> s) & 1u);
+          drain_wait(bar_sffull + 8 * s, (fill_phase >> s) & 1u);
+        }
   } else if (warp >= 2 && warp < kFirstEpiWarp) {
     // ---------------------------------------------------------------- scale warps
     const int q = warp & 3;                               // TMEM lane quadrant of this warp
@@ -282,26 +312,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
       for (int kb = 0; kb < kblocks; ++kb) {
-        const int nk = min(4, ksteps - kb * 4);
         // every lane waits, then the warp agrees (the stores below are warp-wide)
-        ok = wait_bounded(bar_full + 8 * stage, phase, abort_flag, p.wait_limit_ns, p.status, 5);
+        ok = wait_bounded(bar_sffull + 8 * stage, phase, abort_flag, p.wait_limit_ns, p.status, 5);
         ok = __all_sync(0xFFFFFFFFu, ok);
         if (!ok) break;
-        const uint32_t sfa_t = tmem + lanes + SF_TMEM0 + stage * SF_SLOT;
-        const uint32_t sfb_t = sfa_t + SFA_COLS;
-        const uint8_t* ssfa = smem + OFF_SFA + stage * SFA_BYTES + lane * 16;
+        // Atom layout: 16-byte chunk `lane` of a 512-byte atom holds rows lane,
+        // lane+32, lane+64, lane+96 (4 bytes each, one per 16-element block).
+        // Every k-step slot is written, also past the last one of a K tail: the
+        // MMAs never read those columns, and the stale bytes stay in bounds.
+        const uint8_t* ssfa = smem + OFF_SFA + stage * SFA_BYTES + lane * 16 + q * 4;
         const uint8_t* ssfb = smem + OFF_SFB + stage * SFB_BYTES + lane * 16;
-        for (int kk = 0; kk < nk; ++kk) {
-          // atom layout: chunk `lane` of a 512-byte atom holds rows lane, lane+32,
-          // lane+64, lane+96 (4 bytes each); the word of row 32q+lane is word q
-          const uint32_t a_sf = *reinterpret_cast<const uint32_t*>(ssfa + kk * 512 + q * 4);
+        uint32_t a[4], b[32];
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          a[kk] = *reinterpret_cast<const uint32_t*>(ssfa + kk * 512);    // row 32q + lane
           // B rows lane+32j, j = 0..3 (first 128 rows) and 4..7 (second 128 rows);
           // for a 128-column tile the second half is stale and never read
-          const uint4 b_lo = *reinterpret_cast<const uint4*>(ssfb + kk * 512);
-          const uint4 b_hi = *reinterpret_cast<const uint4*>(ssfb + SFA_BYTES + kk * 512);
-          tc_st_x1(sfa_t + 4 * kk + q, a_sf);
-          tc_st_x8(sfb_t + 8 * kk, b_lo, b_hi);
+          const uint4 lo = *reinterpret_cast<const uint4*>(ssfb + kk * 512);
+          const uint4 hi = *reinterpret_cast<const uint4*>(ssfb + SFA_BYTES + kk * 512);
+          b[8 * kk + 0] = lo.x; b[8 * kk + 1] = lo.y; b[8 * kk + 2] = lo.z; b[8 * kk + 3] = lo.w;
+          b[8 * kk + 4] = hi.x; b[8 * kk + 5] = hi.y; b[8 * kk + 6] = hi.z; b[8 * kk + 7] = hi.w;
         }
+        const uint32_t sfa_t = tmem + lanes + SFA_TMEM0 + stage * SFA_SLOT + q;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) tc_st1(sfa_t + 4 * kk, a[kk]);
+        tc_st32(tmem + lanes + SFB_TMEM0 + stage * SFB_SLOT, b);
         tc_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -316,31 +351,48 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- MMA issuer
     uint32_t stage = 0, phase = 0, aphase = 0;
     bool ok = true, issued = false;
+    // Only the weight-tile width changes between tiles, and only when N is not a
+    // multiple of 256; otherwise the issuer never decodes a tile (decoding reads
+    // global memory, which would leave the tensor pipe idle at tile boundaries).
+    const bool uniform_n = p.N % BN == 0;
+    const uint64_t adesc0 = sdesc_kmajor_sw128(sbase);
+    const uint64_t bdesc0 = sdesc_kmajor_sw128(sbase + OFF_B);
     if (p.test_stall && blockIdx.x < total)
       ok = wait_bounded(bar_never, 0, abort_flag, p.wait_limit_ns, p.status, 6);
     for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-      int e, nb, mb, rows, ncols;
-      sch.decode(t, e, nb, mb, rows, ncols);
-      const uint32_t idesc = idesc_nvf4(BM, ncols);
+      uint32_t idesc = idesc_nvf4(BM, BN);
+      if (!uniform_n) {
+        int e, nb, mb, rows, ncols;
+        sch.decode(t, e, nb, mb, rows, ncols);
+        idesc = idesc_nvf4(BM, ncols);
+      }
       if (!wait_bounded(bar_acce, aphase ^ 1, abort_flag, p.wait_limit_ns, p.status, 2)) {
         ok = false;
         break;
       }
       tc_fence_after();
       for (int kb = 0; kb < kblocks; ++kb) {
-        const int nk = min(4, ksteps - kb * 4);
-        if (!wait_bounded(bar_sfready + 8 * stage, phase, abort_flag, p.wait_limit_ns, p.status, 3)) {
+        if (!wait_bounded(bar_sfready + 8 * stage, phase, abort_flag, p.wait_limit_ns, p.status, 3) ||
+            !wait_bounded(bar_full + 8 * stage, phase, abort_flag, p.wait_limit_ns, p.status, 7)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t sfa_t = tmem + SF_TMEM0 + stage * SF_SLOT;
-        const uint32_t sfb_t = sfa_t + SFA_COLS;
-        const uint32_t sa = sbase + stage * A_BYTES;
-        const uint32_t sb = sbase + OFF_B + stage * B_BYTES;
-        for (int kk = 0; kk < nk; ++kk)
-          tc_mma_nvf4(tmem, sdesc_kmajor_sw128(sa + kk * 32), sdesc_kmajor_sw128(sb + kk * 32), idesc,
-                      sfa_t + 4 * kk, sfb_t + 8 * kk, (kb | kk) != 0 ? 1u : 0u);
+        const uint32_t sfa_t = tmem + SFA_TMEM0 + stage * SFA_SLOT;
+        const uint32_t sfb_t = tmem + SFB_TMEM0 + stage * SFB_SLOT;
+        // descriptor start addresses advance by 32 bytes (64 FP4 codes) per k-step
+        const uint64_t ad = adesc0 + ((stage * A_BYTES) >> 4);
+        const uint64_t bd = bdesc0 + ((stage * B_BYTES) >> 4);
+        if (kb * 4 + 4 <= ksteps) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_nvf4(tmem, ad + 2 * kk, bd + 2 * kk, idesc, sfa_t + 4 * kk, sfb_t + 8 * kk,
+                        (kb | kk) != 0 ? 1u : 0u);
+        } else {
+          for (int kk = 0; kk < ksteps - kb * 4; ++kk)
+            tc_mma_nvf4(tmem, ad + 2 * kk, bd + 2 * kk, idesc, sfa_t + 4 * kk, sfb_t + 8 * kk,
+                        (kb | kk) != 0 ? 1u : 0u);
+        }
         issued = true;
         tc_commit(bar_empty + 8 * stage);
         if (++stage == STAGES) {
@@ -374,17 +426,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool active = row < rows && half * 128 < ncols;
       const float alpha = active ? 1.0f / (gs_a * p.gs_b[e]) : 0.0f;
       if constexpr (!kSwiGLU) {
-        // BF16 output: each 32-column chunk is scaled and packed as it leaves
+        // BF16 output: each 64-column half is scaled and packed as it leaves
         // TMEM (64 registers instead of 128), then the accumulator is released
         uint32_t packed[64];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float v[32];
-          tc_ld32_wait(taddr + 32 * c, v);
+        for (int c = 0; c < 2; ++c) {
+          uint32_t v[64];
+          tc_ld64_wait(taddr + 64 * c, v);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * i] * alpha, v[2 * i + 1] * alpha);
-            packed[16 * c + i] = *reinterpret_cast<uint32_t*>(&b);
+          for (int i = 0; i < 32; ++i) {
+            __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(v[2 * i]) * alpha,
+                                                     __uint_as_float(v[2 * i + 1]) * alpha);
+            packed[32 * c + i] = *reinterpret_cast<uint32_t*>(&b);
           }
         }
         tc_fence_before();
@@ -396,9 +449,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < 16; ++j)
           dst[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
       } else {
-        float v[128];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tc_ld32_wait(taddr + 32 * c, v + 32 * c);
+        uint32_t u[2][64];
+        tc_ld64_wait(taddr, u[0]);
+        tc_ld64_wait(taddr + 64, u[1]);
+        const float* v = reinterpret_cast<const float*>(u);
         tc_fence_before();
         mbar_arrive(bar_acce);
         if (!active) continue;

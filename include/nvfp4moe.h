@@ -220,6 +220,8 @@ int moe_quantize_dispatch(const void* x, int64_t T, int64_t K, int64_t ldx, int 
  *            accumulation rounded once to BF16; leading dimension ldc.
  * Requires K % 64 == 0, N % 128 == 0, 1 <= E <= 1024, a_rows >=
  * nvfp4moe_padded_rows(offsets[E], E); 16-byte aligned pointers, ldc % 8 == 0.
+ * C is written in whole 32-byte sectors when C is 32-byte aligned and
+ * ldc % 16 == 0 (faster), else in 16-byte pieces.
  */
 int nvfp4_grouped_gemm(const uint8_t* a_codes, const uint8_t* a_sf, const float* gs_a,
                        int64_t a_rows, const uint8_t* b_codes, const uint8_t* b_sf,
@@ -235,8 +237,9 @@ int nvfp4_grouped_gemm(const uint8_t* a_codes, const uint8_t* a_sf, const float*
  * quantize_activation_nvfp4 with pre-computed gs; "Fused SwiGLU - Remaining
  * Steps" 2-4: quantize in the epilogue and store FP4 + scales straight into
  * the padded L2 input).
- *   h_codes  a_rows x I/2 bytes, h_sf NVFP4_SF_TILED for (a_rows, I), in the
- *            same grouped-padded rows as A (padding rows are not written).
+ *   h_codes  a_rows x I/2 bytes (32-byte aligned), h_sf NVFP4_SF_TILED for
+ *            (a_rows, I), in the same grouped-padded rows as A (padding rows
+ *            are not written).
  * Requires I % 64 == 0, K % 64 == 0, 1 <= E <= 1024.
  */
 int nvfp4_grouped_gemm_swiglu(const uint8_t* a_codes, const uint8_t* a_sf, const float* gs_a,

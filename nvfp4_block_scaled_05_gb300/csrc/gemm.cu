@@ -90,6 +90,7 @@ struct Params {
   // plain epilogue
   __nv_bfloat16* c;
   int64_t ldc;
+  int c_32B;                  // c and ldc allow 32-byte stores
   // SwiGLU epilogue
   uint8_t* h_codes;
   uint8_t* h_sf;
@@ -444,10 +445,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(bar_acce);
         if (!active) continue;
         const int64_t orow = (int64_t)p.offsets[e] + mb * BM + row;
-        uint4* dst = reinterpret_cast<uint4*>(p.c + orow * p.ldc + nb * BN + half * 128);
+        __nv_bfloat16* out = p.c + orow * p.ldc + nb * BN + half * 128;
+        // whole 32-byte sectors when the output allows it: a warp's stores go to
+        // 32 different rows, and half-sector writes double the store requests
+        if (p.c_32B) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          dst[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+          for (int j = 0; j < 8; ++j)
+            st_global_32B(out + 16 * j, packed[8 * j], packed[8 * j + 1], packed[8 * j + 2], packed[8 * j + 3],
+                          packed[8 * j + 4], packed[8 * j + 5], packed[8 * j + 6], packed[8 * j + 7]);
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(out);
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            dst[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+        }
       } else {
         uint32_t u[2][64];
         tc_ld64_wait(taddr, u[0]);
@@ -474,9 +485,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sf = quantize_block16(h, gs_h, words[2 * b], words[2 * b + 1]);
           sfw |= sf << (8 * b);
         }
-        uint4* dst = reinterpret_cast<uint4*>(p.h_codes + hrow * (p.I / 2) + hfeat / 2);
-        dst[0] = make_uint4(words[0], words[1], words[2], words[3]);
-        dst[1] = make_uint4(words[4], words[5], words[6], words[7]);
+        uint8_t* hc = p.h_codes + hrow * (p.I / 2) + hfeat / 2;   // 32-byte aligned (I % 64 == 0)
+        st_global_32B(hc, words[0], words[1], words[2], words[3], words[4], words[5], words[6], words[7]);
         *reinterpret_cast<uint32_t*>(p.h_sf + sf_tiled_offset(hrow, hfeat / 16, p.I / 64)) = sfw;
       }
     }
@@ -604,6 +614,7 @@ extern "C" int nvfp4_grouped_gemm(const uint8_t* a_codes, const uint8_t* a_sf, c
   p.b_sf_expert_bytes = (int64_t)nvfp4_sf_bytes(N, K, NVFP4_SF_TILED);
   p.c = static_cast<__nv_bfloat16*>(c);
   p.ldc = ldc;
+  p.c_32B = aligned(c, 32) && ldc % 16 == 0;
   return launch_grouped<false>(a_codes, a_rows, b_codes, (int)N, (int)K, p, as_stream(stream));
 }
 
@@ -615,7 +626,7 @@ extern "C" int nvfp4_grouped_gemm_swiglu(const uint8_t* a_codes, const uint8_t* 
                                          void* stream) {
   NVFP4_CHECK(I > 0 && I % 64 == 0, NVFP4MOE_ERR_UNSUPPORTED);
   NVFP4_TRY(check_common(a_codes, a_sf, gs_a, a_rows, w1_codes, w1_sf, gs_w1, offsets, E, 2 * I, K));
-  NVFP4_CHECK(gs_h && h_codes && h_sf && aligned(h_codes, 16) && aligned(h_sf, 16), NVFP4MOE_ERR_INVALID);
+  NVFP4_CHECK(gs_h && h_codes && h_sf && aligned(h_codes, 32) && aligned(h_sf, 16), NVFP4MOE_ERR_INVALID);
   Params p{};
   p.a_sf = a_sf;
   p.b_sf = w1_sf;

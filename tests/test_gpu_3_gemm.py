@@ -55,7 +55,7 @@ def _rand_q(rng, rows, cols, std, mode="random"):
     return c, s, gs
 
 
-def _run_grouped(rng, counts, N, K, mode_a="random", mode_b="random", name="g"):
+def _run_grouped(rng, counts, N, K, mode_a="random", mode_b="random", name="g", wide=False):
     E = len(counts)
     offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
     M = int(offsets[-1])
@@ -75,8 +75,12 @@ def _run_grouped(rng, counts, N, K, mode_a="random", mode_b="random", name="g"):
     d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
     a_sf_t = _tile_sf(asf_rm, a_rows, K)
     b_sf_t = np.concatenate([_tile_sf(bsf[e], N, K) for e in range(E)])
+    out = None
+    if wide:
+        # a 16-byte-offset view with ldc % 16 != 0: the 16-byte store path
+        out = torch.zeros((max(M, 1), N + 24), dtype=torch.bfloat16, device=DEV)[:M, 8:8 + N]
     c = B.nvfp4_grouped_gemm(d(a_pad), d(a_sf_t), d(np.array([gsa], np.float32)), d(bc), d(b_sf_t),
-                             d(gsb), d(offsets))
+                             d(gsb), d(offsets), out=out)
     st = B.nvfp4moe_last_device_status()
     got = c.float().cpu().numpy()
     ok = st == 0 and np.all(np.abs(got - ref) <= 2e-2 * np.maximum(1.0, np.abs(ref)))
@@ -109,6 +113,15 @@ def test_k_tails(K):
     got, ref = _run_grouped(rng, [40, 200], 128, K, name="k%d" % K)
     assert_close_north_star(got, ref, "K=%d" % K)
     assert cosine(got, ref) > 0.9999
+
+
+def test_strided_output_matches_sector_path():
+    """The same GEMM into a 16-byte-offset, odd-stride output view (16-byte
+    stores) gives the same bits as into a packed output (32-byte stores)."""
+    got_w, ref = _run_grouped(np.random.default_rng(11), [70, 0, 200], 256, 512, name="wide", wide=True)
+    got_p, _ = _run_grouped(np.random.default_rng(11), [70, 0, 200], 256, 512, name="packed")
+    assert np.array_equal(got_w, got_p)
+    assert_close_north_star(got_w, ref, "wide")
 
 
 def test_linear_workload_sampled_rows():

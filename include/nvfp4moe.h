@@ -248,6 +248,31 @@ int nvfp4_grouped_gemm_swiglu(const uint8_t* a_codes, const uint8_t* a_sf, const
                               int64_t K, const float* gs_h, uint8_t* h_codes, uint8_t* h_sf,
                               void* stream);
 
+/* Workspace bytes nvfp4_linear needs (the row bounds of its single group). */
+size_t nvfp4_linear_workspace_size(void);
+
+/*
+ * nvfp4_linear -- one NVFP4 x NVFP4 linear with BF16 output, for shared
+ * experts and projections (README "NVFP4 Linear": CuTeDSLNvfp4Linear, a
+ * single-expert NVFP4 GEMM): C[m, n] = sum_k A[m, k] * W[n, k] / (gs_a * gs_w)
+ * for m < M, f32 accumulation rounded once to BF16. It is the grouped GEMM
+ * with one group, so it can run on its own stream beside the routed experts.
+ *   A   a_rows x K/2 codes, row-major (nvfp4_quantize output), with
+ *       a_rows >= 128 * ceil(M / 128) allocated rows (rows >= M are read and
+ *       their products discarded), scales NVFP4_SF_TILED for (a_rows, K),
+ *       global scale *gs_a (device).
+ *   W   N x K/2 codes, scales NVFP4_SF_TILED for (N, K), *gs_w (device).
+ *   C   M x N BF16, leading dimension ldc (alignment as nvfp4_grouped_gemm).
+ *   ws  >= nvfp4_linear_workspace_size() bytes, 16-byte aligned, device; it
+ *       holds the group bounds and must not be shared by calls in flight.
+ * Requires K % 64 == 0, N % 128 == 0. Errors as nvfp4_grouped_gemm, plus
+ * WORKSPACE.
+ */
+int nvfp4_linear(const uint8_t* a_codes, const uint8_t* a_sf, const float* gs_a, int64_t M,
+                 int64_t a_rows, const uint8_t* w_codes, const uint8_t* w_sf, const float* gs_w,
+                 int64_t N, int64_t K, void* c, int64_t ldc, void* ws, size_t ws_bytes,
+                 void* stream);
+
 /*
  * moe_combine -- stage 6 (README "MoE Runner" step 6, scatter with routing
  * weights): y[t, :] = sum_{j<k} topk_w[t, j] * out[flat_to_perm[t*k + j], :],

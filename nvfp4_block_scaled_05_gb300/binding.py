@@ -52,6 +52,9 @@ _SIGS = {
     "moe_forward": (_int, [_c_void_p, _c_void_p, _i64, _i64, _i64, _int, _int, _c_void_p,
                            _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
                            _c_void_p, _c_void_p, _size, _c_void_p]),
+    "nvfp4_linear_workspace_size": (_size, []),
+    "nvfp4_linear": (_int, [_c_void_p, _c_void_p, _c_void_p, _i64, _i64, _c_void_p, _c_void_p, _c_void_p,
+                            _i64, _i64, _c_void_p, _i64, _c_void_p, _size, _c_void_p]),
     "nvfp4moe_last_device_status": (_int, [_c_void_p]),
     "nvfp4moe_set_wait_limit_ns": (None, [ctypes.c_uint64]),
     "nvfp4moe_set_test_stall": (None, [_int]),
@@ -241,6 +244,21 @@ def nvfp4_grouped_gemm(a_codes, a_sf, gs_a, b_codes, b_sf, gs_b, offsets, out=No
     _check(lib().nvfp4_grouped_gemm(_ptr(a_codes), _ptr(a_sf), _ptr(gs_a), a_codes.shape[0],
                                     _ptr(b_codes), _ptr(b_sf), _ptr(gs_b), _ptr(offsets), E, N, K,
                                     _ptr(out), out.stride(0), _stream()), "nvfp4_grouped_gemm")
+    return out
+
+
+def nvfp4_linear(a_codes, a_sf, gs_a, M, w_codes, w_sf, gs_w, out=None, ws=None):
+    """A (a_rows >= 128*ceil(M/128), K/2) x W (N, K/2) -> C (M, N) BF16."""
+    N, khalf = w_codes.shape
+    K = khalf * 2
+    dev = a_codes.device
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    if ws is None:
+        ws = torch.empty(int(lib().nvfp4_linear_workspace_size()), dtype=torch.uint8, device=dev)
+    _check(lib().nvfp4_linear(_ptr(a_codes), _ptr(a_sf), _ptr(gs_a), M, a_codes.shape[0], _ptr(w_codes),
+                              _ptr(w_sf), _ptr(gs_w), N, K, _ptr(out), out.stride(0), _ptr(ws), ws.numel(),
+                              _stream()), "nvfp4_linear")
     return out
 
 

@@ -146,3 +146,31 @@ extern "C" int moe_forward(const void* x, const float* router_logits, int64_t T,
   NVFP4_TRY(moe_combine(out, K, topw, f2p, T, k, K, y, K, stream));
   return NVFP4MOE_OK;
 }
+
+// ------------------------------------------------------------------ single linear
+
+namespace {
+__global__ void linear_bounds_kernel(int32_t* bounds, int32_t M) {
+  bounds[0] = 0;
+  bounds[1] = M;
+}
+}  // namespace
+
+extern "C" size_t nvfp4_linear_workspace_size(void) { return 256; }
+
+extern "C" int nvfp4_linear(const uint8_t* a_codes, const uint8_t* a_sf, const float* gs_a, int64_t M,
+                            int64_t a_rows, const uint8_t* w_codes, const uint8_t* w_sf,
+                            const float* gs_w, int64_t N, int64_t K, void* c, int64_t ldc, void* ws,
+                            size_t ws_bytes, void* stream) {
+  NVFP4_CHECK(M >= 0 && M < (1ll << 31), NVFP4MOE_ERR_UNSUPPORTED);
+  if (M == 0) return NVFP4MOE_OK;
+  NVFP4_CHECK(a_rows >= ceil_div(M, 128) * 128, NVFP4MOE_ERR_INVALID);
+  NVFP4_CHECK(ws && ws_bytes >= nvfp4_linear_workspace_size() && aligned(ws, 16), NVFP4MOE_ERR_WORKSPACE);
+  cudaStream_t s = as_stream(stream);
+  int32_t* bounds = static_cast<int32_t*>(ws);
+  linear_bounds_kernel<<<1, 1, 0, s>>>(bounds, (int32_t)M);
+  NVFP4_TRY(launch_status());
+  // one group of M rows: its padded rows are the rows themselves
+  return nvfp4_grouped_gemm(a_codes, a_sf, gs_a, a_rows, w_codes, w_sf, gs_w, bounds, 1, N, K, c, ldc,
+                            stream);
+}

@@ -16,6 +16,10 @@ Shapes and distributions follow the five workloads the kernels are measured on:
 * ``prefill``  T=8192,  same layer shape
 * ``skewed``   T=16384, same layer shape, Zipf(1.2) expert popularity over a
                seeded permutation of the experts, 16 seeded experts never chosen
+* ``dsv4_decode`` / ``dsv4_prefill``  T=128 / 8192, K=7168, I=3072, E=384,
+               top-6, uniform routing: the DeepSeek-V4 routed-expert shape the
+               pages name ("NVFP4 MegaMoE Kernel" README, model notes: 384
+               experts, top-6, intermediate 3072)
 
 x ~ N(0, 1) BF16, router logits ~ N(0, 1) f32 (the top-k of iid logits is a
 uniformly random k-subset), weights ~ N(0, 0.02) BF16. W1 is drawn as (E, 2I, K)
@@ -77,6 +81,10 @@ CONFIGS = {
     "prefill": MoEConfig("prefill", T=8192, K=7168, I=2048, E=256, k=8, gs_h=28.0),
     "skewed": MoEConfig("skewed", T=16384, K=7168, I=2048, E=256, k=8, routing="zipf",
                         zipf_s=1.2, n_dead=16, gs_h=28.0),
+    # the h distribution depends on K and the weight scale, not on I, so the
+    # same pre-computed gs_h leaves h unsaturated
+    "dsv4_decode": MoEConfig("dsv4_decode", T=128, K=7168, I=3072, E=384, k=6, gs_h=28.0),
+    "dsv4_prefill": MoEConfig("dsv4_prefill", T=8192, K=7168, I=3072, E=384, k=6, gs_h=28.0),
     # profiler-sized cases: the same layer and the same rows per expert as
     # prefill / decode, with 32 experts (0.8 GB of weights, still above L2)
     "prefill_small": MoEConfig("prefill_small", T=1024, K=7168, I=2048, E=32, k=8, gs_h=28.0),

@@ -1,5 +1,6 @@
 """GPU parity of the whole MoE forward (moe_forward through the C ABI) against
-the oracle, on the five workloads' MoE shapes.
+the oracle, on the workloads' MoE shapes (including the DeepSeek-V4 routed-expert
+shape).
 
 tiny: every token; decode/prefill/skewed: the routing, the permutation and the
 quantized activations of every token are compared bit for bit, and the output
@@ -89,6 +90,13 @@ def test_moe_decode_sampled():
 @pytest.mark.parametrize("name", ["prefill", "skewed"])
 def test_moe_prefill_shapes_sampled(name):
     _run(W.CONFIGS[name], 0, 3)
+
+
+@pytest.mark.parametrize("name,sample", [("dsv4_decode", 4), ("dsv4_prefill", 2)])
+def test_moe_deepseek_v4_shape_sampled(name, sample):
+    """384 experts, top-6, I=3072: the routed-expert shape of the model the
+    pages deploy (gate/up N = 6144, down-projection K = 3072)."""
+    _run(W.CONFIGS[name], 0, sample)
 
 
 def test_moe_edge_shapes():

@@ -32,6 +32,7 @@ METRIC = "MoE layer TFLOP/s & tokens/s at 1 GB300; % of FP4 tensor peak / HBM BW
 FP4_OVER_BF16 = 13.5 / 2.25        # nominal dense FP4 / dense BF16 tensor rate
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNELS_PER_STEP = 10              # route 1, permute 3, quantize 3, L1 1, L2 1, combine 1
+KERNELS_PER_STEP_STATIC = 4        # fused dispatch 1, L1 1, L2 1, combine 1
 
 
 def parse_args():
@@ -47,6 +48,10 @@ def parse_args():
     ap.add_argument("--cpu-experts", type=int, default=8,
                     help="experts whose routed rows form the CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--front", default="split", choices=["split", "static"],
+                    help="split: route/permute/quantize kernels with gs_x computed every step; "
+                         "static: moe_forward_static (one fused front kernel, gs_x pre-computed once)")
+    ap.add_argument("--graph", action="store_true", help="replay the step as a captured CUDA graph")
     return ap.parse_args()
 
 
@@ -317,9 +322,40 @@ def run_ours(args, cfg):
         if pg is not None:
             pg.barrier()
 
-    # ---- device-resident timing of moe_forward
-    for _ in range(args.warmup):
+    static = args.front == "static"
+    gs_x = None
+    if static:
+        # the pre-computed activation scale: one calibration forward's gs_x
         B.moe_forward(x, logits, wts, k, gs_h, ws=ws, y=y)
+        lay0 = B.moe_forward_workspace_layout(T, K, I, E, k)
+        gs_x = ws[lay0["gs_x"]:lay0["gs_x"] + 4].view(torch.float32).clone()
+
+    def forward(xx, ll):
+        if static:
+            B.moe_forward_static(xx, ll, wts, k, gs_h, gs_x, ws=ws, y=y)
+        else:
+            B.moe_forward(xx, ll, wts, k, gs_h, ws=ws, y=y)
+
+    def captured(xx, ll):
+        """forward(xx, ll) as a replayable CUDA graph (or None without --graph)."""
+        if not args.graph:
+            return None
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            forward(xx, ll)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                forward(xx, ll)
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        return g
+
+    # ---- device-resident timing of the forward
+    graph = captured(x, logits)
+    run = graph.replay if graph is not None else (lambda: forward(x, logits))
+    for _ in range(args.warmup):
+        run()
     st = B.nvfp4moe_last_device_status()
     if st != 0:
         raise RuntimeError("device status %d after warm-up" % st)
@@ -331,7 +367,7 @@ def run_ours(args, cfg):
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
     for _ in range(args.steps):
-        B.moe_forward(x, logits, wts, k, gs_h, ws=ws, y=y)
+        run()
     ev1.record(stream)
     barrier()
     t_end = time.time()
@@ -341,24 +377,30 @@ def run_ours(args, cfg):
         raise RuntimeError("device status after timed region")
 
     # ---- per-stage device time (same stream, events between the six calls)
-    nst = len(B.STAGES)
+    names = B.STATIC_STAGES if static else B.STAGES
+    nst = len(names)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(args.steps)]
     barrier()
     for i in range(args.steps):
-        B.moe_forward_stages(x, logits, wts, k, gs_h, ws, y, events=evs[i])
+        if static:
+            B.moe_forward_static_stages(x, logits, wts, k, gs_h, gs_x, ws, y, events=evs[i])
+        else:
+            B.moe_forward_stages(x, logits, wts, k, gs_h, ws, y, events=evs[i])
     barrier()
     stage_ms = {name: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)) / args.steps
-                for j, name in enumerate(B.STAGES)}
+                for j, name in enumerate(names)}
 
     # ---- end to end through the public call, host buffers, copies timed
     x_h = x.cpu().pin_memory()
     l_h = logits.cpu().pin_memory()
     y_h = torch.empty((T, K), dtype=torch.bfloat16).pin_memory()
     x_d, l_d = torch.empty_like(x), torch.empty_like(logits)
+    graph_e2e = captured(x_d, l_d)
+    run_e2e = graph_e2e.replay if graph_e2e is not None else (lambda: forward(x_d, l_d))
     for _ in range(max(1, args.warmup // 2)):
         x_d.copy_(x_h, non_blocking=True)
         l_d.copy_(l_h, non_blocking=True)
-        B.moe_forward(x_d, l_d, wts, k, gs_h, ws=ws, y=y)
+        run_e2e()
         y_h.copy_(y, non_blocking=True)
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -366,7 +408,7 @@ def run_ours(args, cfg):
     for _ in range(args.steps):
         x_d.copy_(x_h, non_blocking=True)
         l_d.copy_(l_h, non_blocking=True)
-        B.moe_forward(x_d, l_d, wts, k, gs_h, ws=ws, y=y)
+        run_e2e()
         y_h.copy_(y, non_blocking=True)
     e1.record(stream)
     barrier()
@@ -412,6 +454,9 @@ def run_ours(args, cfg):
         "config": {"workload": cfg.name, "T": T, "K": K, "I": I, "E": E, "k": k, "M": cfg.M,
                    "global_tokens": world * T, "parallelism": "replicas x%d" % world,
                    "active_experts": nums["active"], "seed": args.seed, "gs_h": cfg.gs_h,
+                   "front": ("static (moe_forward_static; gs_x pre-computed once by a calibration "
+                             "forward)" if static else "split (gs_x computed every step)"),
+                   "cuda_graph": bool(args.graph),
                    "l2": "inputs larger than L2: %.2f GB of expert weights streamed every step"
                          % (nums["bytes"] / 1e9)},
         "tokens_per_s": tokens_s,
@@ -423,7 +468,7 @@ def run_ours(args, cfg):
         "e2e": {"value": world * nums["flops"] / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": x.numel() * 2 + logits.numel() * 4,
                 "d2h_bytes_per_step": y.numel() * 2},
-        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "gpu_launches": (KERNELS_PER_STEP_STATIC if static else KERNELS_PER_STEP) * args.steps,
         "clocks": clk,
     }
     if world == 1 and not args.no_cpu_baseline:

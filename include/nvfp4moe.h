@@ -143,7 +143,7 @@ int nvfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx,
  * descending logit, and softmax weights over those k logits (f32, expf).
  *   logits  (T, E) f32 row-major.  topk_ids (T, k) int32, topk_w (T, k) f32.
  * Supports 1 <= k <= 16, k <= E <= 1024. Logits may be -inf (never chosen
- * before a finite one); NaN logits are not supported.
+ * before a finite one); a NaN logit ranks below every other logit (as -inf).
  */
 int moe_route_topk(const float* logits, int64_t T, int E, int k,
                    int32_t* topk_ids, float* topk_w, void* stream);
@@ -317,8 +317,52 @@ int moe_forward(const void* x, const float* router_logits, int64_t T, int64_t K,
                 const float* gs_w2, const float* gs_h, void* y, void* ws, size_t ws_bytes,
                 void* stream);
 
+/* Workspace bytes moe_dispatch_static needs (T >= 1). */
+size_t moe_dispatch_static_workspace_size(int64_t T, int E);
+
+/*
+ * moe_dispatch_static -- stages 1 and 2 fused, with a pre-computed activation
+ * global scale *gs_x (README "Bridge Layer": quantize_activation_nvfp4 with
+ * pre-computed gs; "MoE Runner" steps 1-2): moe_route_topk, moe_permute and
+ * moe_quantize_dispatch (with gs_in = gs_x) in ONE cooperative kernel with
+ * two grid-wide barriers, each bounded by the wait limit (a timeout sets the
+ * device status; offsets and flat_to_perm are then all zero).
+ * Outputs as those three calls: topk_ids / topk_w (T, k); offsets (E + 1);
+ * perm_to_flat / flat_to_perm (T*k); a_codes / a_sf in the grouped-padded
+ * rows of (a_rows, K) with a_rows >= nvfp4moe_padded_rows(T*k, E).
+ * ws >= moe_dispatch_static_workspace_size(T, E) bytes, 256-byte aligned.
+ * Requires K % 64 == 0, 1 <= k <= 16, k <= E <= 1024, and T * k <= 4096 * G
+ * (G = co-resident blocks of the kernel, at least one per SM).
+ */
+int moe_dispatch_static(const void* x, int64_t ldx, const float* router_logits, int64_t T,
+                        int64_t K, int E, int k, const float* gs_x, int32_t* topk_ids,
+                        float* topk_w, int32_t* offsets, int32_t* perm_to_flat,
+                        int32_t* flat_to_perm, uint8_t* a_codes, uint8_t* a_sf, int64_t a_rows,
+                        void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * moe_forward_static -- moe_forward with a pre-computed activation global
+ * scale (README "Bridge Layer": quantize_activation_nvfp4, the CUDA-graph-safe
+ * quantizer with a pre-computed gs; "CUDAGraph-safe": workspace pre-allocated,
+ * no runtime allocation): moe_dispatch_static (routing, permutation,
+ * quantization and scatter as one kernel), then the L1, L2 and combine
+ * kernels of moe_forward.
+ *   gs_x  device f32: the global scale x is quantized with (codes and scales
+ *         as nvfp4_quantize with gs_in = gs_x). Values of |x| * gs_x beyond
+ *         the E4M3 x E2M1 range saturate.
+ * Other arguments, workspace and layout as moe_forward; the intermediates sit
+ * at the same workspace offsets (the gs_x slot is not written). Also needs
+ * T * k <= 4096 * G, G the co-resident blocks of the front kernel (at least
+ * one per SM: 77 824 tokens at k = 8 on 152 SMs); UNSUPPORTED beyond.
+ */
+int moe_forward_static(const void* x, const float* router_logits, int64_t T, int64_t K, int64_t I,
+                       int E, int k, const float* gs_x, const uint8_t* w1_codes,
+                       const uint8_t* w1_sf, const float* gs_w1, const uint8_t* w2_codes,
+                       const uint8_t* w2_sf, const float* gs_w2, const float* gs_h, void* y,
+                       void* ws, size_t ws_bytes, void* stream);
+
 /* Waits for `stream`, then reads and clears the device status word that the
- * GEMM kernels set when a bounded wait runs out (README "Key Lessons" 5: no
+ * GEMM and fused-front kernels set when a bounded wait runs out (README "Key Lessons" 5: no
  * silent failure). Returns NVFP4MOE_OK, NVFP4MOE_ERR_DEVICE_TIMEOUT or
  * NVFP4MOE_ERR_LAUNCH (a CUDA error on the stream). */
 int nvfp4moe_last_device_status(void* stream);
@@ -330,7 +374,9 @@ void nvfp4moe_set_wait_limit_ns(uint64_t ns);
 /* Test hook for the failure path: while set (non-zero), the MMA-issuing
  * thread of every GEMM CTA that has work first waits on a barrier that
  * nothing arrives on, so that bounded wait runs out after the wait limit and
- * the kernel takes its abort path. Host only; affects launches made
+ * the kernel takes its abort path; and block 0 of the fused front
+ * (moe_forward_static) leaves before its first grid barrier, so the other
+ * blocks' bounded barrier waits run out. Host only; affects launches made
  * afterwards. */
 void nvfp4moe_set_test_stall(int on);
 

@@ -52,6 +52,13 @@ _SIGS = {
     "moe_forward": (_int, [_c_void_p, _c_void_p, _i64, _i64, _i64, _int, _int, _c_void_p,
                            _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
                            _c_void_p, _c_void_p, _size, _c_void_p]),
+    "moe_forward_static": (_int, [_c_void_p, _c_void_p, _i64, _i64, _i64, _int, _int, _c_void_p,
+                                  _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                                  _c_void_p, _c_void_p, _c_void_p, _size, _c_void_p]),
+    "moe_dispatch_static_workspace_size": (_size, [_i64, _int]),
+    "moe_dispatch_static": (_int, [_c_void_p, _i64, _c_void_p, _i64, _i64, _int, _int, _c_void_p, _c_void_p,
+                                   _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _i64,
+                                   _c_void_p, _size, _c_void_p]),
     "nvfp4_linear_workspace_size": (_size, []),
     "nvfp4_linear": (_int, [_c_void_p, _c_void_p, _c_void_p, _i64, _i64, _c_void_p, _c_void_p, _c_void_p,
                             _i64, _i64, _c_void_p, _i64, _c_void_p, _size, _c_void_p]),
@@ -306,6 +313,23 @@ def moe_forward(x, logits, weights, k, gs_h, ws=None, y=None):
     return y
 
 
+def moe_forward_static(x, logits, weights, k, gs_h, gs_x, ws=None, y=None):
+    """moe_forward with a pre-computed activation global scale gs_x (device
+    f32); the front (route, permute, quantize, scatter) is one kernel."""
+    T, K = x.shape
+    E = logits.shape[1]
+    I = weights["I"]
+    if ws is None:
+        ws = torch.empty(moe_forward_workspace_size(T, K, I, E, k), dtype=torch.uint8, device=x.device)
+    if y is None:
+        y = torch.empty((T, K), dtype=torch.bfloat16, device=x.device)
+    _check(lib().moe_forward_static(_ptr(x), _ptr(logits), T, K, I, E, k, _ptr(gs_x),
+                                    _ptr(weights["w1_codes"]), _ptr(weights["w1_sf"]), _ptr(weights["gs_w1"]),
+                                    _ptr(weights["w2_codes"]), _ptr(weights["w2_sf"]), _ptr(weights["gs_w2"]),
+                                    _ptr(gs_h), _ptr(y), _ptr(ws), ws.numel(), _stream()), "moe_forward_static")
+    return y
+
+
 def prepare_moe_weights(w1, w2, free_source=False):
     """Offline weight preparation through nvfp4_quantize (README "Bridge Layer":
     quantize_weight_to_nvfp4, interleave_l1_weights, make_b_k_major).
@@ -336,6 +360,7 @@ def prepare_moe_weights(w1, w2, free_source=False):
 
 
 STAGES = ("route", "permute", "quantize", "l1_swiglu", "l2", "combine")
+STATIC_STAGES = ("dispatch_static", "l1_swiglu", "l2", "combine")
 
 
 def moe_forward_stages(x, logits, weights, k, gs_h, ws, y, events=None):
@@ -386,4 +411,47 @@ def moe_forward_stages(x, logits, weights, k, gs_h, ws, y, events=None):
     _check(L.moe_combine(p["out"], K, p["topk_w"], p["flat_to_perm"], T, k, K, _ptr(y), y.stride(0), s),
            "combine")
     mark(6)
+    return y
+
+
+def moe_forward_static_stages(x, logits, weights, k, gs_h, gs_x, ws, y, events=None):
+    """The four C calls moe_forward_static makes (moe_dispatch_static, L1, L2,
+    combine) issued one by one with the same workspace carving; events[i] is
+    recorded before stage i (len(STATIC_STAGES) + 1 events)."""
+    T, K = x.shape
+    E = logits.shape[1]
+    I = weights["I"]
+    L = lib()
+    lay = moe_forward_workspace_layout(T, K, I, E, k)
+    base = ws.data_ptr()
+    p = {n: ctypes.c_void_p(base + o) for n, o in lay.items() if n != "a_rows"}
+    a_rows = lay["a_rows"]
+    M = T * k
+    up = lambda v: -(-v // 256) * 256
+    front_off = lay["out"] + up(M * K * 2)
+    front_ws = base + front_off
+    front_bytes = ws.numel() - front_off
+    s = _stream()
+    st = torch.cuda.current_stream()
+
+    def mark(i):
+        if events is not None:
+            events[i].record(st)
+
+    mark(0)
+    _check(L.moe_dispatch_static(_ptr(x), K, _ptr(logits), T, K, E, k, _ptr(gs_x), p["topk_ids"], p["topk_w"],
+                                 p["offsets"], p["perm_to_flat"], p["flat_to_perm"], p["a_codes"], p["a_sf"],
+                                 a_rows, ctypes.c_void_p(front_ws), front_bytes, s), "dispatch_static")
+    mark(1)
+    _check(L.nvfp4_grouped_gemm_swiglu(p["a_codes"], p["a_sf"], _ptr(gs_x), a_rows,
+                                       _ptr(weights["w1_codes"]), _ptr(weights["w1_sf"]),
+                                       _ptr(weights["gs_w1"]), p["offsets"], E, I, K, _ptr(gs_h),
+                                       p["h_codes"], p["h_sf"], s), "l1_swiglu")
+    mark(2)
+    _check(L.nvfp4_grouped_gemm(p["h_codes"], p["h_sf"], _ptr(gs_h), a_rows, _ptr(weights["w2_codes"]),
+                                _ptr(weights["w2_sf"]), _ptr(weights["gs_w2"]), p["offsets"], E, K, I,
+                                p["out"], K, s), "l2")
+    mark(3)
+    _check(L.moe_combine(p["out"], K, p["topk_w"], p["flat_to_perm"], T, k, K, _ptr(y), K, s), "combine")
+    mark(4)
     return y

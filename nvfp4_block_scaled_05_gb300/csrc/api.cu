@@ -75,10 +75,12 @@ Layout make_layout(int64_t T, int64_t K, int64_t I, int E, int k) {
   L.off[9] = take((int64_t)nvfp4_sf_bytes(a_rows, I, NVFP4_SF_TILED));
   L.off[10] = take(M * K * 2);
   L.off[11] = a_rows;
-  const int64_t perm_ws = take((int64_t)moe_permute_workspace_size(T, k, E));
-  const int64_t disp_ws = take((int64_t)moe_quantize_dispatch_workspace_size(E));
-  (void)perm_ws;
-  (void)disp_ws;
+  // scratch: the permute and dispatch workspaces (moe_forward), or the fused
+  // front's (moe_forward_static), whichever is larger
+  const int64_t split = up256((int64_t)moe_permute_workspace_size(T, k, E)) +
+                        up256((int64_t)moe_quantize_dispatch_workspace_size(E));
+  const int64_t front = (int64_t)front_workspace_bytes(T, E);
+  take(split > front ? split : front);
   L.total = o;
   return L;
 }
@@ -145,6 +147,67 @@ extern "C" int moe_forward(const void* x, const float* router_logits, int64_t T,
                                I, out, K, stream));
   NVFP4_TRY(moe_combine(out, K, topw, f2p, T, k, K, y, K, stream));
   return NVFP4MOE_OK;
+}
+
+extern "C" int moe_forward_static(const void* x, const float* router_logits, int64_t T, int64_t K,
+                                  int64_t I, int E, int k, const float* gs_x, const uint8_t* w1_codes,
+                                  const uint8_t* w1_sf, const float* gs_w1, const uint8_t* w2_codes,
+                                  const uint8_t* w2_sf, const float* gs_w2, const float* gs_h, void* y,
+                                  void* ws, size_t ws_bytes, void* stream) {
+  NVFP4_CHECK(forward_shape_ok(T, K, I, E, k), NVFP4MOE_ERR_UNSUPPORTED);
+  if (T == 0) return NVFP4MOE_OK;
+  NVFP4_CHECK(x && router_logits && gs_x && w1_codes && w1_sf && gs_w1 && w2_codes && w2_sf && gs_w2 &&
+                  gs_h && y && aligned(x, 16),
+              NVFP4MOE_ERR_INVALID);
+  const Layout L = make_layout(T, K, I, E, k);
+  NVFP4_CHECK(ws && ws_bytes >= (size_t)L.total && aligned(ws, 256), NVFP4MOE_ERR_WORKSPACE);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int32_t* ids = reinterpret_cast<int32_t*>(w + L.off[0]);
+  float* topw = reinterpret_cast<float*>(w + L.off[1]);
+  int32_t* offsets = reinterpret_cast<int32_t*>(w + L.off[2]);
+  int32_t* p2f = reinterpret_cast<int32_t*>(w + L.off[3]);
+  int32_t* f2p = reinterpret_cast<int32_t*>(w + L.off[4]);
+  uint8_t* a_codes = w + L.off[6];
+  uint8_t* a_sf = w + L.off[7];
+  uint8_t* h_codes = w + L.off[8];
+  uint8_t* h_sf = w + L.off[9];
+  void* out = w + L.off[10];
+  const int64_t a_rows = L.off[11];
+  const int64_t M = T * k;
+  uint8_t* front_ws = w + L.off[10] + up256(M * K * 2);
+  const size_t front_bytes = (size_t)(L.total - (L.off[10] + up256(M * K * 2)));
+  NVFP4_TRY(moe_dispatch_static(x, K, router_logits, T, K, E, k, gs_x, ids, topw, offsets, p2f, f2p,
+                                a_codes, a_sf, a_rows, front_ws, front_bytes, stream));
+  NVFP4_TRY(nvfp4_grouped_gemm_swiglu(a_codes, a_sf, gs_x, a_rows, w1_codes, w1_sf, gs_w1, offsets,
+                                      E, I, K, gs_h, h_codes, h_sf, stream));
+  NVFP4_TRY(nvfp4_grouped_gemm(h_codes, h_sf, gs_h, a_rows, w2_codes, w2_sf, gs_w2, offsets, E, K,
+                               I, out, K, stream));
+  NVFP4_TRY(moe_combine(out, K, topw, f2p, T, k, K, y, K, stream));
+  return NVFP4MOE_OK;
+}
+
+extern "C" size_t moe_dispatch_static_workspace_size(int64_t T, int E) {
+  if (T < 1 || E < 1 || E > 1024) return 0;
+  return front_workspace_bytes(T, E);
+}
+
+extern "C" int moe_dispatch_static(const void* x, int64_t ldx, const float* router_logits, int64_t T,
+                                   int64_t K, int E, int k, const float* gs_x, int32_t* topk_ids,
+                                   float* topk_w, int32_t* offsets, int32_t* perm_to_flat,
+                                   int32_t* flat_to_perm, uint8_t* a_codes, uint8_t* a_sf,
+                                   int64_t a_rows, void* ws, size_t ws_bytes, void* stream) {
+  NVFP4_CHECK(T >= 0 && K > 0 && K % 64 == 0 && k >= 1 && k <= 16 && E >= k && E <= 1024 &&
+                  T * k < (1ll << 31),
+              NVFP4MOE_ERR_UNSUPPORTED);
+  if (T == 0) return NVFP4MOE_OK;
+  NVFP4_CHECK(x && router_logits && gs_x && topk_ids && topk_w && offsets && perm_to_flat &&
+                  flat_to_perm && a_codes && a_sf,
+              NVFP4MOE_ERR_INVALID);
+  NVFP4_CHECK(ldx >= K && ldx % 8 == 0 && aligned(x, 16) && aligned(a_codes, 8) && aligned(a_sf, 4),
+              NVFP4MOE_ERR_INVALID);
+  NVFP4_CHECK(a_rows >= nvfp4moe_padded_rows(T * k, E), NVFP4MOE_ERR_INVALID);
+  return moe_front(x, ldx, router_logits, T, K, E, k, gs_x, topk_ids, topk_w, offsets, perm_to_flat,
+                   flat_to_perm, a_codes, a_sf, ws, ws_bytes, as_stream(stream));
 }
 
 // ------------------------------------------------------------------ single linear

@@ -36,6 +36,20 @@ inline int launch_status() {
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Library-wide device state (defined with the GEMM): the device status word
+// (int[2]: status, wait site), the bound on every device-side wait, the SM
+// count, the failure-path test hook.
+int* device_status_word();
+uint64_t wait_limit_ns();
+int device_num_sms();
+int test_stall_on();   // failure-path test hook (nvfp4moe_set_test_stall)
+
+// Fused front of moe_forward_static (front.cu).
+size_t front_workspace_bytes(int64_t T, int E);
+int moe_front(const void* x, int64_t ldx, const float* logits, int64_t T, int64_t K, int E, int k,
+              const float* gs_x, int32_t* ids, float* w, int32_t* offsets, int32_t* p2f, int32_t* f2p,
+              uint8_t* a_codes, uint8_t* a_sf, void* ws, size_t ws_bytes, cudaStream_t s);
+
 // Byte offset of the scale of (row r, 16-element block b) in the tiled layout
 // documented in nvfp4moe.h.
 __host__ __device__ inline int64_t sf_tiled_offset(int64_t r, int64_t b, int64_t c4) {
@@ -111,6 +125,82 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float* f) {
     f[2 * i] = __uint_as_float(w[i] << 16);
     f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
   }
+}
+
+// Router step for one token, one warp ("MoE Runner" step 1 input: top-k of
+// the router logits, softmax over the k selected). Each lane holds VPL logits
+// (expert lane + 32*i); ties go to the lower expert index; the k winners are
+// in descending order. Lane j < k receives winner j's expert and weight.
+template <int VPL>
+__device__ __forceinline__ void route_token(const float* __restrict__ row, int E, int k, int lane,
+                                            int& my_i, float& my_w) {
+  float v[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = e < E ? row[e] : -INFINITY;
+    if (v[i] != v[i]) v[i] = -INFINITY;  // a NaN logit is never preferred (and never leaves no choice)
+  }
+  uint32_t taken = 0;
+  float my_v = -INFINITY;
+  my_i = 0;
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int bi = 0x7FFFFFFF;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
+        bv = v[i];
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
+      const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
+      if (ov > bv || (ov == bv && oi < bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (lane == j) {
+      my_v = bv;
+      my_i = bi;
+    }
+  }
+  // softmax over the k selected logits; the first selected is the maximum
+  const float vmax = __shfl_sync(0xFFFFFFFFu, my_v, 0);
+  const float ex = lane < k ? expf(my_v - vmax) : 0.0f;
+  float den = ex;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xFFFFFFFFu, den, o);
+  my_w = ex / den;
+}
+
+// Quantize the 16 BF16 elements at x_row[col0 .. col0+15] (zeros when x_row
+// is null); returns the scale byte, the codes in w0/w1.
+__device__ __forceinline__ uint32_t quantize_lane16(const __nv_bfloat16* x_row, int64_t col0, float gs,
+                                                    uint32_t& w0, uint32_t& w1) {
+  float v[16];
+  if (x_row) {
+    const uint4* p = reinterpret_cast<const uint4*>(x_row + col0);
+    bf16x8_to_f32(__ldg(p), v);
+    bf16x8_to_f32(__ldg(p + 1), v + 8);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = 0.0f;
+  }
+  return quantize_block16(v, gs, w0, w1);
+}
+
+// The scale bytes of lanes 4q..4q+3 as one little-endian word (valid in lane 4q).
+__device__ __forceinline__ uint32_t gather_sf_word(uint32_t sf) {
+  const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, sf, 1);
+  const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, sf, 2);
+  const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, sf, 3);
+  return sf | (b1 << 8) | (b2 << 16) | (b3 << 24);
 }
 
 // ------------------------------------------------------------------ PTX wrappers

@@ -1,0 +1,324 @@
+// Fused front of the MoE forward with a pre-computed activation global scale
+// ("NVFP4 MegaMoE Kernel" README, "Bridge Layer": quantize_activation_nvfp4,
+// the CUDA-graph-safe quantizer with a pre-computed gs; "MoE Runner" steps 1
+// and 2): routing, the stable permutation, NVFP4 quantization and the scatter
+// into the padded L1 operand, in one cooperative launch.
+//
+// G blocks; block c owns the contiguous tokens [c*tpb, (c+1)*tpb) and so the
+// contiguous flat slots [c*tpb*k, (c+1)*tpb*k).
+//   phase 1  route the block's tokens (one warp per token) and histogram
+//            their experts -> counts[c][e]
+//   -- grid barrier --
+//   phase 2  block c turns the columns e = c, c+G, ... into exclusive prefixes
+//            over blocks (counts[c'][e] = slots of expert e in blocks < c')
+//            and writes the column total
+//   -- grid barrier --
+//   phase 3  every block: exclusive scans of the totals -> offsets (block 0
+//            writes them) and padded group starts; the stable position of
+//            each of its slots (one warp, 32 slots at a time, grouped with
+//            __match_any_sync), then each token row is quantized once and
+//            written to the padded rows of its k slots.
+// The same permutation as moe_permute (a stable counting sort by expert of
+// the flat slots t*k + j), the same rows as moe_quantize_dispatch.
+//
+// The grid barriers are bounded: one that does not complete within the wait
+// limit sets the device status to NVFP4MOE_ERR_DEVICE_TIMEOUT (wait site 8 or
+// 9) and the kernel returns. Offsets and flat_to_perm are zeroed before the first barrier, so
+// the later stages then find no rows and read nothing out of bounds.
+#include "common.cuh"
+
+namespace nvfp4moe {
+namespace {
+
+constexpr int kFrontThreads = 512;
+constexpr int kFrontMaxSlots = 4096;   // flat slots per block (tpb * k)
+constexpr int kFrontMaxBlocks = 1024;
+
+struct FrontParams {
+  const __nv_bfloat16* x;
+  int64_t ldx;
+  const float* logits;
+  int64_t T;
+  int K, E, k, tpb;
+  const float* gs_x;
+  int32_t* ids;
+  float* w;
+  int32_t* offsets;
+  int32_t* p2f;
+  int32_t* f2p;
+  uint8_t* a_codes;
+  uint8_t* a_sf;
+  int32_t* counts;        // [G][E]
+  int32_t* totals;        // [E]
+  unsigned int* barrier;  // zeroed before the launch
+  uint64_t limit_ns;
+  int* status;
+  int test_stall;         // block 0 leaves before the first grid barrier
+};
+
+__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// All blocks of the (cooperative) grid arrive; false if the wait timed out.
+__device__ bool grid_barrier(const FrontParams& p, unsigned int target, int site, int* flag) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(p.barrier, 1u);
+    int ok = 1;
+    const uint64_t t0 = global_timer_ns();
+    while (ld_acquire_gpu(p.barrier) < target) {
+      if (global_timer_ns() - t0 > p.limit_ns) {
+        ok = 0;
+        if (atomicCAS(&p.status[0], 0, NVFP4MOE_ERR_DEVICE_TIMEOUT) == 0) p.status[1] = site;
+        break;
+      }
+    }
+    *flag = ok;
+  }
+  __syncthreads();
+  return *flag != 0;
+}
+
+// Block-wide exclusive scan of n <= 2 * kFrontThreads values in place (smem).
+__device__ void block_exclusive_scan(int32_t* a, int n, int32_t* warp_tot) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int i0 = 2 * tid, i1 = 2 * tid + 1;
+  const int v0 = i0 < n ? a[i0] : 0, v1 = i1 < n ? a[i1] : 0;
+  const int pair = v0 + v1;
+  int incl = pair;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int y = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+    if (lane >= d) incl += y;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int s = lane < kFrontThreads / 32 ? warp_tot[lane] : 0;
+    int si = s;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, si, d);
+      if (lane >= d) si += y;
+    }
+    if (lane < kFrontThreads / 32) warp_tot[lane] = si - s;
+  }
+  __syncthreads();
+  const int excl = warp_tot[warp] + incl - pair;
+  if (i0 < n) a[i0] = excl;
+  if (i1 < n) a[i1] = excl + v0;
+  __syncthreads();
+}
+
+template <int VPL>
+__global__ void __launch_bounds__(kFrontThreads) moe_front_kernel(const FrontParams p) {
+  extern __shared__ int32_t sm[];
+  const int E = p.E, k = p.k;
+  int32_t* next = sm;                    // [E]
+  int32_t* offs = next + E;              // [E + 1]
+  int32_t* pad = offs + (E + 1);         // [E + 1]
+  int32_t* slot_e = pad + (E + 1);       // [tpb * k]
+  int32_t* slot_pos = slot_e + p.tpb * k;
+  int32_t* misc = slot_pos + p.tpb * k;  // [32]: warp totals, barrier flag
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = kFrontThreads / 32;
+  const int G = gridDim.x, c = blockIdx.x;
+  const int64_t t0 = (int64_t)c * p.tpb;
+  const int64_t t1 = t0 + p.tpb < p.T ? t0 + p.tpb : p.T;
+  const int ntok = t1 > t0 ? (int)(t1 - t0) : 0;
+  const int nslot = ntok * k;
+
+  // ---- phase 1: route, histogram; safe offsets / flat_to_perm first
+  for (int e = tid; e < E; e += kFrontThreads) next[e] = 0;
+  if (c == 0)
+    for (int e = tid; e <= E; e += kFrontThreads) p.offsets[e] = 0;
+  for (int s = tid; s < nslot; s += kFrontThreads) p.f2p[t0 * k + s] = 0;
+  __syncthreads();
+  for (int tl = warp; tl < ntok; tl += nwarps) {
+    const int64_t t = t0 + tl;
+    int my_i;
+    float my_w;
+    route_token<VPL>(p.logits + t * E, E, k, lane, my_i, my_w);
+    if (lane < k) {
+      p.ids[t * k + lane] = my_i;
+      p.w[t * k + lane] = my_w;
+      slot_e[tl * k + lane] = my_i;
+      atomicAdd(&next[my_i], 1);
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += kFrontThreads) p.counts[(int64_t)c * E + e] = next[e];
+  if (p.test_stall && c == 0) return;
+  if (!grid_barrier(p, (unsigned)G, 8, misc + 31)) return;
+
+  // ---- phase 2: per expert column, exclusive prefix over blocks and total
+  for (int e = c + G * warp; e < E; e += G * nwarps) {
+    int carry = 0;
+    for (int base = 0; base < G; base += 32) {
+      const int cc = base + lane;
+      const int v = cc < G ? __ldcg(p.counts + (int64_t)cc * E + e) : 0;
+      int incl = v;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+        if (lane >= d) incl += y;
+      }
+      if (cc < G) p.counts[(int64_t)cc * E + e] = carry + incl - v;
+      carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    }
+    if (lane == 0) p.totals[e] = carry;
+  }
+  if (!grid_barrier(p, 2u * G, 9, misc + 31)) return;
+
+  // ---- phase 3: offsets, padded starts, stable positions, quantize + scatter
+  for (int e = tid; e < E; e += kFrontThreads) {
+    const int n = __ldcg(p.totals + e);
+    offs[e] = n;
+    pad[e] = (n + 127) / 128 * 128;
+  }
+  __syncthreads();
+  block_exclusive_scan(offs, E, misc);
+  block_exclusive_scan(pad, E, misc);
+  if (c == 0) {
+    for (int e = tid; e < E; e += kFrontThreads) p.offsets[e] = offs[e];
+    if (tid == 0) p.offsets[E] = (int32_t)(p.T * k);
+  }
+  for (int e = tid; e < E; e += kFrontThreads) next[e] = offs[e] + __ldcg(p.counts + (int64_t)c * E + e);
+  __syncthreads();
+  if (warp == 0) {
+    for (int i = 0; i < nslot; i += 32) {
+      const int s = i + lane;
+      const bool valid = s < nslot;
+      const int e = valid ? slot_e[s] : -1 - lane;  // invalid lanes never match a real expert
+      const uint32_t peers = __match_any_sync(0xFFFFFFFFu, e);
+      const int rank = __popc(peers & ((1u << lane) - 1u));
+      const int start = valid ? next[e] : 0;
+      __syncwarp();
+      if (valid) {
+        const int pos = start + rank;
+        const int64_t f = t0 * k + s;
+        slot_pos[s] = pos;
+        p.p2f[pos] = (int32_t)f;
+        p.f2p[f] = pos;
+        if (lane == 31 - __clz(peers)) next[e] = start + __popc(peers);
+      }
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  const float gs = *p.gs_x;
+  const int nchunk = (p.K + 511) / 512;
+  const int64_t c4 = p.K / 64;
+  for (int item = warp; item < ntok * nchunk; item += nwarps) {
+    const int tl = item / nchunk;
+    const int64_t col0 = (int64_t)(item - tl * nchunk) * 512 + lane * 16;
+    const bool valid = col0 < p.K;
+    uint32_t w0 = 0, w1 = 0, s = 0;
+    if (valid) s = quantize_lane16(p.x + (t0 + tl) * p.ldx, col0, gs, w0, w1);
+    const uint32_t word = gather_sf_word(s);
+    for (int j = 0; j < k; ++j) {
+      const int e = slot_e[tl * k + j];
+      const int64_t prow = (int64_t)pad[e] + slot_pos[tl * k + j] - offs[e];
+      if (valid) *reinterpret_cast<uint2*>(p.a_codes + prow * (p.K / 2) + col0 / 2) = make_uint2(w0, w1);
+      if (valid && (lane & 3) == 0)
+        *reinterpret_cast<uint32_t*>(p.a_sf + sf_tiled_offset(prow, col0 / 16, c4)) = word;
+    }
+  }
+}
+
+size_t front_smem_bytes(int E, int slots) { return (size_t)(3 * E + 2 + 2 * slots + 32) * 4; }
+
+template <int VPL>
+int launch_front_vpl(FrontParams& p, int G, size_t smem, cudaStream_t s) {
+  auto kern = moe_front_kernel<VPL>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return NVFP4MOE_ERR_LAUNCH;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)G);
+  cfg.blockDim = dim3(kFrontThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return NVFP4MOE_ERR_LAUNCH;
+  return launch_status();
+}
+
+template <int VPL>
+int max_coresident(size_t smem) {
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, moe_front_kernel<VPL>, kFrontThreads, smem) !=
+      cudaSuccess)
+    return 0;
+  return per_sm * device_num_sms();
+}
+
+int vpl_of(int E) { return E <= 32 ? 1 : E <= 64 ? 2 : E <= 128 ? 4 : E <= 256 ? 8 : E <= 512 ? 16 : 32; }
+
+}  // namespace
+
+size_t front_workspace_bytes(int64_t T, int E) {
+  const int64_t g = T < kFrontMaxBlocks ? T : kFrontMaxBlocks;
+  return 256 + (size_t)ceil_div((int64_t)E * 4, 256) * 256 + (size_t)ceil_div(g * E * 4, 256) * 256;
+}
+
+int moe_front(const void* x, int64_t ldx, const float* logits, int64_t T, int64_t K, int E, int k,
+              const float* gs_x, int32_t* ids, float* w, int32_t* offsets, int32_t* p2f, int32_t* f2p,
+              uint8_t* a_codes, uint8_t* a_sf, void* ws, size_t ws_bytes, cudaStream_t s) {
+  NVFP4_CHECK(T >= 1 && K % 64 == 0 && k >= 1 && k <= 16 && k <= E && E <= 1024, NVFP4MOE_ERR_UNSUPPORTED);
+  NVFP4_CHECK(ws && ws_bytes >= front_workspace_bytes(T, E) && aligned(ws, 256), NVFP4MOE_ERR_WORKSPACE);
+  const size_t smem_max = front_smem_bytes(E, kFrontMaxSlots);
+  const int vpl = vpl_of(E);
+  int gmax = vpl == 1 ? max_coresident<1>(smem_max) : vpl == 2 ? max_coresident<2>(smem_max)
+           : vpl == 4 ? max_coresident<4>(smem_max) : vpl == 8 ? max_coresident<8>(smem_max)
+           : vpl == 16 ? max_coresident<16>(smem_max) : max_coresident<32>(smem_max);
+  if (gmax > kFrontMaxBlocks) gmax = kFrontMaxBlocks;
+  NVFP4_CHECK(gmax >= 1, NVFP4MOE_ERR_LAUNCH);
+  int G = (int)(T < gmax ? T : gmax);
+  const int tpb = (int)ceil_div(T, G);
+  G = (int)ceil_div(T, tpb);
+  NVFP4_CHECK((int64_t)tpb * k <= kFrontMaxSlots, NVFP4MOE_ERR_UNSUPPORTED);
+  FrontParams p{};
+  p.x = static_cast<const __nv_bfloat16*>(x);
+  p.ldx = ldx;
+  p.logits = logits;
+  p.T = T;
+  p.K = (int)K;
+  p.E = E;
+  p.k = k;
+  p.tpb = tpb;
+  p.gs_x = gs_x;
+  p.ids = ids;
+  p.w = w;
+  p.offsets = offsets;
+  p.p2f = p2f;
+  p.f2p = f2p;
+  p.a_codes = a_codes;
+  p.a_sf = a_sf;
+  uint8_t* wb = static_cast<uint8_t*>(ws);
+  p.barrier = reinterpret_cast<unsigned int*>(wb);
+  p.totals = reinterpret_cast<int32_t*>(wb + 256);
+  p.counts = reinterpret_cast<int32_t*>(wb + 256 + ceil_div((int64_t)E * 4, 256) * 256);
+  p.limit_ns = wait_limit_ns();
+  p.status = device_status_word();
+  p.test_stall = test_stall_on();
+  NVFP4_CHECK(p.status, NVFP4MOE_ERR_LAUNCH);
+  if (cudaMemsetAsync(p.barrier, 0, sizeof(unsigned int), s) != cudaSuccess) return NVFP4MOE_ERR_LAUNCH;
+  const size_t smem = front_smem_bytes(E, tpb * k);
+  switch (vpl) {
+    case 1: return launch_front_vpl<1>(p, G, smem, s);
+    case 2: return launch_front_vpl<2>(p, G, smem, s);
+    case 4: return launch_front_vpl<4>(p, G, smem, s);
+    case 8: return launch_front_vpl<8>(p, G, smem, s);
+    case 16: return launch_front_vpl<16>(p, G, smem, s);
+    default: return launch_front_vpl<32>(p, G, smem, s);
+  }
+}
+
+}  // namespace nvfp4moe

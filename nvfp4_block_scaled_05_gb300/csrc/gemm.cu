@@ -591,6 +591,18 @@ int check_common(const uint8_t* a_codes, const uint8_t* a_sf, const float* gs_a,
 }
 
 }  // namespace
+
+int* device_status_word() {
+  int* status = nullptr;
+  return cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_status) == cudaSuccess ? status : nullptr;
+}
+
+uint64_t wait_limit_ns() { return g_wait_limit_ns; }
+
+int device_num_sms() { return num_sms(); }
+
+int test_stall_on() { return g_test_stall; }
+
 }  // namespace nvfp4moe
 
 using namespace nvfp4moe;

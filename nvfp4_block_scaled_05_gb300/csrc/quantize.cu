@@ -43,30 +43,6 @@ __device__ __forceinline__ float load_gs(const float* gs_in, const uint32_t* ama
   return gs_in ? *gs_in : global_scale_from_amax_bits(*amax_bits);
 }
 
-// Quantize the 16 elements at x_row[col0 .. col0+15] (zeros when x_row is null).
-__device__ __forceinline__ uint32_t quantize_lane(const __nv_bfloat16* x_row, int64_t col0, float gs,
-                                                  uint32_t& w0, uint32_t& w1) {
-  float v[16];
-  if (x_row) {
-    const uint4* p = reinterpret_cast<const uint4*>(x_row + col0);
-    bf16x8_to_f32(__ldg(p), v);
-    bf16x8_to_f32(__ldg(p + 1), v + 8);
-  } else {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = 0.0f;
-  }
-  return quantize_block16(v, gs, w0, w1);
-}
-
-// Gather the scale bytes of lanes 4q..4q+3 into one little-endian word.
-__device__ __forceinline__ uint32_t gather_sf_word(uint32_t sf, int lane) {
-  const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, sf, 1);
-  const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, sf, 2);
-  const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, sf, 3);
-  (void)lane;
-  return sf | (b1 << 8) | (b2 << 16) | (b3 << 24);
-}
-
 __global__ void __launch_bounds__(256) quantize_rows_kernel(
     const __nv_bfloat16* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx,
     const float* gs_in, const uint32_t* amax_bits, float* gs_out,
@@ -83,10 +59,10 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(
   const bool valid = col0 < cols;
   const int64_t src = row_src ? (int64_t)row_src[r] : r;
   uint32_t w0 = 0, w1 = 0, s = 0;
-  if (valid) s = quantize_lane(src >= 0 ? x + src * ldx : nullptr, col0, gs, w0, w1);
+  if (valid) s = quantize_lane16(src >= 0 ? x + src * ldx : nullptr, col0, gs, w0, w1);
   if (valid) *reinterpret_cast<uint2*>(codes + r * (cols / 2) + col0 / 2) = make_uint2(w0, w1);
   if (sf_layout == NVFP4_SF_TILED) {
-    const uint32_t word = gather_sf_word(s, lane);
+    const uint32_t word = gather_sf_word(s);
     if (valid && (lane & 3) == 0)
       *reinterpret_cast<uint32_t*>(sf + sf_tiled_offset(r, col0 / 16, (cols + 63) / 64)) = word;
   } else if (valid) {
@@ -132,8 +108,8 @@ __global__ void __launch_bounds__(256) dispatch_quantize_kernel(
   const int64_t col0 = (gw - t * nchunk) * kChunk + lane * 16;
   const bool valid = col0 < K;
   uint32_t w0 = 0, w1 = 0, s = 0;
-  if (valid) s = quantize_lane(x + t * ldx, col0, gs, w0, w1);
-  const uint32_t word = gather_sf_word(s, lane);
+  if (valid) s = quantize_lane16(x + t * ldx, col0, gs, w0, w1);
+  const uint32_t word = gather_sf_word(s);
   const int64_t c4 = K / 64;
   for (int j = 0; j < k; ++j) {
     const int64_t f = t * k + j;

@@ -29,50 +29,12 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
   const int lane = threadIdx.x & 31;
   const int64_t t = blockIdx.x * (int64_t)(blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
-  float v[VPL];
-#pragma unroll
-  for (int i = 0; i < VPL; ++i) {
-    const int e = lane + 32 * i;
-    v[i] = e < E ? logits[t * E + e] : -INFINITY;
-  }
-  uint32_t taken = 0;
-  float my_v = -INFINITY;
-  int my_i = 0;
-  for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int bi = 0x7FFFFFFF;
-#pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
-        bv = v[i];
-        bi = e;
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
-      const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
-      if (ov > bv || (ov == bv && oi < bi)) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    if (lane == j) {
-      my_v = bv;
-      my_i = bi;
-    }
-  }
-  // softmax over the k selected logits; the first selected is the maximum
-  const float vmax = __shfl_sync(0xFFFFFFFFu, my_v, 0);
-  const float ex = lane < k ? expf(my_v - vmax) : 0.0f;
-  float den = ex;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xFFFFFFFFu, den, o);
+  int my_i;
+  float my_w;
+  route_token<VPL>(logits + t * E, E, k, lane, my_i, my_w);
   if (lane < k) {
     ids[t * k + lane] = my_i;
-    w[t * k + lane] = ex / den;
+    w[t * k + lane] = my_w;
   }
 }
 

@@ -254,7 +254,7 @@ def quantize_expert(w_bf16: np.ndarray):
 
 
 def moe_forward(x, logits, get_w1, get_w2, k, gs_h, tokens=None, keep=False, experts=None,
-                qweights=None):
+                qweights=None, gs_x=None):
     """README "MoE Runner", steps 1-6, for the tokens listed in ``tokens``.
 
     x: (T, K) BF16 bits; logits: (T, E) f32; get_w1(e) -> (2I, K) BF16 bits with
@@ -268,7 +268,10 @@ def moe_forward(x, logits, get_w1, get_w2, k, gs_h, tokens=None, keep=False, exp
     the expert work to the routed rows of those experts, so y then holds only
     their share of the weighted sum. ``qweights`` (optional) maps an expert to
     its already-quantized (c1, s1, g1, c2, s2, g2), skipping the offline weight
-    quantization. Returns a dict with the routing, the permutation, gs_x,
+    quantization. ``gs_x`` (optional) is a pre-computed activation global scale
+    (README "Bridge Layer": quantize_activation_nvfp4 with pre-computed gs,
+    the CUDA-graph-safe path); by default gs_x = 2688 / amax|x| over all T
+    tokens. Returns a dict with the routing, the permutation, gs_x,
     y (len(tokens), K) fp64, and per-(token, j) intermediates when ``keep``.
     """
     T, K = x.shape
@@ -276,7 +279,7 @@ def moe_forward(x, logits, get_w1, get_w2, k, gs_h, tokens=None, keep=False, exp
     ids, w = route_topk(logits, k)
     offsets, p2f, f2p = permute(ids, E)
     amax_x = amax_bf16(x)
-    gs_x = global_scale(amax_x)
+    gs_x = global_scale(amax_x) if gs_x is None else np.float32(gs_x)
     tokens = list(range(T)) if tokens is None else [int(t) for t in tokens]
     xc, xs = quantize_bf16(np.ascontiguousarray(x[tokens]), gs_x)
     xd = dequantize_f64(xc, xs, gs_x)

@@ -1,0 +1,156 @@
+"""GPU parity of moe_forward_static: the forward with a pre-computed activation
+global scale, whose route + permute + quantize + scatter run as one
+cooperative kernel.
+
+* With gs_x equal to the one moe_forward computes, every intermediate (routing,
+  permutation, offsets, the quantized rows) and y are bit-identical to
+  moe_forward's.
+* With another gs_x, the intermediates equal the oracle's (given that gs_x) bit
+  for bit and y is within the tolerance.
+* Captured in a CUDA graph and replayed on new inputs, it gives the eager
+  result bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from helpers import assert_close_north_star, cosine, padded_rows_of_compact, sf_tiled_index
+from nvfp4_block_scaled_05_gb300 import binding as B
+from nvfp4_block_scaled_05_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+NAMES = ["topk_ids", "topk_w", "offsets", "perm_to_flat", "flat_to_perm"]
+
+
+def _view(ws, lay, name, dtype, count):
+    off = lay[name]
+    n = torch.empty((), dtype=dtype).element_size()
+    return ws[off:off + count * n].view(dtype)
+
+
+def _inter(ws, lay, T, K, E, k):
+    M = T * k
+    d = {n: _view(ws, lay, n, torch.int32 if n != "topk_w" else torch.float32, E + 1 if n == "offsets" else M)
+         .cpu().numpy().copy() for n in NAMES}
+    a_rows = lay["a_rows"]
+    prow = padded_rows_of_compact(d["offsets"])
+    codes = _view(ws, lay, "a_codes", torch.uint8, a_rows * K // 2).view(a_rows, K // 2).cpu().numpy()
+    sf = _view(ws, lay, "a_sf", torch.uint8, B.nvfp4_sf_bytes(a_rows, K)).cpu().numpy()
+    d["rows"] = codes[prow]
+    d["sf"] = sf[sf_tiled_index(a_rows, K)][prow]
+    return d
+
+
+def _setup(cfg, seed=0):
+    inp = W.moe_inputs(cfg, seed=seed, device=DEV)
+    wts = B.prepare_moe_weights(inp["w1"], inp["w2"])
+    gs_h = torch.tensor([cfg.gs_h], dtype=torch.float32, device=DEV)
+    nb = B.moe_forward_workspace_size(cfg.T, cfg.K, cfg.I, cfg.E, cfg.k)
+    lay = B.moe_forward_workspace_layout(cfg.T, cfg.K, cfg.I, cfg.E, cfg.k)
+    return inp, wts, gs_h, nb, lay
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "prefill", "dsv4_decode"])
+def test_static_equals_dynamic_with_same_gs(name):
+    cfg = W.CONFIGS[name]
+    inp, wts, gs_h, nb, lay = _setup(cfg)
+    ws1 = torch.empty(nb, dtype=torch.uint8, device=DEV)
+    ws2 = torch.full((nb,), 0xAB, dtype=torch.uint8, device=DEV)   # stale bytes
+    y1 = B.moe_forward(inp["x"], inp["logits"], wts, cfg.k, gs_h, ws=ws1)
+    gs_x = _view(ws1, lay, "gs_x", torch.float32, 1).clone()
+    y2 = B.moe_forward_static(inp["x"], inp["logits"], wts, cfg.k, gs_h, gs_x, ws=ws2)
+    assert B.nvfp4moe_last_device_status() == 0
+    a = _inter(ws1, lay, cfg.T, cfg.K, cfg.E, cfg.k)
+    b = _inter(ws2, lay, cfg.T, cfg.K, cfg.E, cfg.k)
+    for n in a:
+        assert np.array_equal(a[n], b[n]), n
+    assert torch.equal(y1, y2)
+
+
+@pytest.mark.parametrize("name,sample", [("tiny", None), ("decode", 4)])
+def test_static_matches_oracle_with_given_gs(name, sample):
+    cfg = W.CONFIGS[name]
+    inp, wts, gs_h, nb, lay = _setup(cfg, seed=1)
+    xb = W.bf16_bits(inp["x"])
+    g = np.float32(O.global_scale(O.amax_bf16(xb)) * np.float32(0.75))   # not the computed one
+    ws = torch.empty(nb, dtype=torch.uint8, device=DEV)
+    y = B.moe_forward_static(inp["x"], inp["logits"], wts, cfg.k, gs_h,
+                             torch.tensor([g], dtype=torch.float32, device=DEV), ws=ws)
+    assert B.nvfp4moe_last_device_status() == 0
+    T, k = cfg.T, cfg.k
+    tokens = (np.arange(T) if sample is None else
+              np.sort(np.random.default_rng(7).choice(T, sample, replace=False)))
+    w1, w2 = inp["w1"], inp["w2"]
+    ref = O.moe_forward(xb, inp["logits"].cpu().numpy(), lambda e: W.bf16_bits(w1[e]),
+                        lambda e: W.bf16_bits(w2[e]), k, np.float32(cfg.gs_h), tokens=tokens, gs_x=g)
+    d = _inter(ws, lay, T, cfg.K, cfg.E, k)
+    assert np.array_equal(d["topk_ids"].reshape(T, k), ref["ids"])
+    assert np.allclose(d["topk_w"].reshape(T, k), ref["w"], rtol=1e-6, atol=1e-7)
+    assert np.array_equal(d["offsets"], ref["offsets"])
+    assert np.array_equal(d["perm_to_flat"], ref["perm_to_flat"])
+    assert np.array_equal(d["flat_to_perm"], ref["flat_to_perm"])
+    f2p = ref["flat_to_perm"]
+    for ti, t in enumerate(ref["tokens"]):
+        for j in range(k):
+            assert np.array_equal(d["rows"][f2p[t * k + j]], ref["x_codes"][ti])
+            assert np.array_equal(d["sf"][f2p[t * k + j]], ref["x_sf"][ti])
+    got = y[torch.from_numpy(np.asarray(ref["tokens"])).to(DEV)].float().cpu().numpy()
+    assert_close_north_star(got, ref["y"], name)
+    assert cosine(got, ref["y"]) >= 0.9995
+
+
+def test_static_edge_shapes():
+    """T=1 (one block), all tokens on one expert, E above the routed rows, and
+    E=1000 (32 logits per lane)."""
+    for (T, K, I, E, k, mode) in [(1, 256, 64, 8, 2, "rand"), (200, 256, 128, 4, 1, "one"),
+                                  (3, 384, 192, 64, 4, "rand"), (700, 128, 64, 1000, 3, "rand")]:
+        cfg = W.MoEConfig("edge", T=T, K=K, I=I, E=E, k=k, gs_h=336.0)
+        g = torch.Generator(device="cpu").manual_seed(T + E)
+        x = torch.randn(T, K, generator=g).to(torch.bfloat16)
+        logits = torch.randn(T, E, generator=g)
+        if mode == "one":
+            logits[:, 2] += 100.0
+        w1 = (torch.randn(E, 2 * I, K, generator=g) * 0.05).to(torch.bfloat16)
+        w2 = (torch.randn(E, K, I, generator=g) * 0.05).to(torch.bfloat16)
+        wts = B.prepare_moe_weights(w1.to(DEV), w2.to(DEV))
+        gs_h = torch.tensor([cfg.gs_h], dtype=torch.float32, device=DEV)
+        nb = B.moe_forward_workspace_size(T, K, I, E, k)
+        ws1 = torch.empty(nb, dtype=torch.uint8, device=DEV)
+        y1 = B.moe_forward(x.to(DEV), logits.to(DEV), wts, k, gs_h, ws=ws1)
+        lay = B.moe_forward_workspace_layout(T, K, I, E, k)
+        gs_x = _view(ws1, lay, "gs_x", torch.float32, 1).clone()
+        ws2 = torch.empty(nb, dtype=torch.uint8, device=DEV)
+        y2 = B.moe_forward_static(x.to(DEV), logits.to(DEV), wts, k, gs_h, gs_x, ws=ws2)
+        assert B.nvfp4moe_last_device_status() == 0
+        a, b = _inter(ws1, lay, T, K, E, k), _inter(ws2, lay, T, K, E, k)
+        for n in a:
+            assert np.array_equal(a[n], b[n]), (n, T, E, k)
+        assert torch.equal(y1, y2), (T, E, k)
+
+
+def test_static_graph_replay_on_new_inputs():
+    cfg = W.CONFIGS["decode"]
+    inp, wts, gs_h, nb, lay = _setup(cfg, seed=2)
+    inp2 = W.moe_inputs(cfg, seed=3, device=DEV, weights=False)
+    gs_x = torch.tensor([2688.0 / 4.5], dtype=torch.float32, device=DEV)
+    ws = torch.empty(nb, dtype=torch.uint8, device=DEV)
+    x_s, l_s = inp["x"].clone(), inp["logits"].clone()
+    y_s = torch.empty_like(inp["x"])
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        B.moe_forward_static(x_s, l_s, wts, cfg.k, gs_h, gs_x, ws=ws, y=y_s)   # warm-up
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            B.moe_forward_static(x_s, l_s, wts, cfg.k, gs_h, gs_x, ws=ws, y=y_s)
+    torch.cuda.current_stream().wait_stream(s)
+    for src in (inp, inp2):
+        x_s.copy_(src["x"])
+        l_s.copy_(src["logits"])
+        graph.replay()
+        torch.cuda.synchronize()
+        eager = B.moe_forward_static(src["x"], src["logits"], wts, cfg.k, gs_h, gs_x)
+        assert B.nvfp4moe_last_device_status() == 0
+        assert torch.equal(y_s, eager)

@@ -176,3 +176,17 @@ def test_moe_forward_single_expert_is_a_two_layer_mlp():
 
 def bf16_bits_np(a):
     return W.bf16_bits(torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16))
+
+
+def test_moe_forward_given_gs_x():
+    """A pre-computed gs_x equal to the computed one changes nothing; another
+    one changes the quantized activations exactly as quantizing x with it."""
+    cfg, x, logits, w1, w2 = _tiny()
+    r = O.moe_forward(x, logits, lambda e: w1[e], lambda e: w2[e], cfg.k, cfg.gs_h)
+    r2 = O.moe_forward(x, logits, lambda e: w1[e], lambda e: w2[e], cfg.k, cfg.gs_h, gs_x=r["gs_x"])
+    assert np.array_equal(r2["y"], r["y"])
+    g = np.float32(r["gs_x"] * 0.5)
+    r3 = O.moe_forward(x, logits, lambda e: w1[e], lambda e: w2[e], cfg.k, cfg.gs_h, gs_x=g)
+    c, s = O.quantize_bf16(x, g)
+    assert r3["gs_x"] == g and np.array_equal(r3["x_codes"], c) and np.array_equal(r3["x_sf"], s)
+    assert not np.array_equal(r3["x_sf"], r["x_sf"])

@@ -52,6 +52,10 @@ def parse_args():
                     help="split: route/permute/quantize kernels with gs_x computed every step; "
                          "static: moe_forward_static (one fused front kernel, gs_x pre-computed once)")
     ap.add_argument("--graph", action="store_true", help="replay the step as a captured CUDA graph")
+    ap.add_argument("--op", default="moe", choices=["moe", "qnorm_rope", "linear"],
+                    help="moe: the expert forward (default); qnorm_rope: the fused RMS norm + RoPE + "
+                         "NVFP4 quantization of attention-head rows; linear: the shared-expert NVFP4 "
+                         "linear (activation quantization + GEMM). The last two: one GPU.")
     return ap.parse_args()
 
 
@@ -479,8 +483,205 @@ def run_ours(args, cfg):
         pg.destroy_process_group()
 
 
+# ---------------------------------------------------------------- side ops
+
+def _timed(stream, steps, fn, flush=None, min_seconds=0.0):
+    """Device ms per call of fn(): CUDA events on `stream` around each call; an
+    optional flush() runs outside the timed spans. At least `steps` calls, and
+    more until `min_seconds` of wall time passed (so the clock sampler sees the
+    timed region). Returns (ms per call, calls)."""
+    import torch
+    total, n = 0.0, 0
+    t0 = time.time()
+    while n < steps or time.time() - t0 < min_seconds:
+        if flush is not None:
+            flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        b.synchronize()
+        total += a.elapsed_time(b)
+        n += 1
+    return total / n, n
+
+
+def _side_line(args, metric, value, unit, ms, config, roof, e2e, launches, clk, cpu, steps):
+    return {"metric": metric, "value": value, "unit": unit, "n_gpus": 1, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "nvfp4 out (e2m1 x e4m3 block scale), f32 arithmetic",
+            "data": "synthetic (seeded)", "config": config, "roofline": roof, "e2e": e2e,
+            "gpu_launches": launches, "clocks": clk, "cpu_baseline": cpu}
+
+
+def run_qnorm_rope(args):
+    """RMS norm -> RoPE -> NVFP4 of q-head rows: T=8192 tokens x 128 heads, head
+    dim 192 (128 plain + 64 rotary), positions = token index, standard RoPE
+    frequencies (base 10000) as f32 tables, pre-computed global scale."""
+    import numpy as np
+    import torch
+    from nvfp4_block_scaled_05_gb300 import binding as B
+    dev = torch.device("cuda", 0)
+    T, H, D, R = 8192, 128, 192, 64
+    rows = T * H
+    g = torch.Generator(device=dev).manual_seed(args.seed)
+    x = torch.randn(rows, D, generator=g, device=dev).to(torch.bfloat16)
+    gamma = (1.0 + 0.1 * torch.randn(D, generator=g, device=dev)).float()
+    inv = 10000.0 ** (-torch.arange(0, R, 2, dtype=torch.float64) / R)
+    ang = torch.arange(T, dtype=torch.float64)[:, None] * inv[None, :]
+    cos_t, sin_t = torch.cos(ang).float().to(dev), torch.sin(ang).float().to(dev)
+    pos = torch.arange(T, dtype=torch.int32, device=dev).repeat_interleave(H)
+    codes = torch.empty((rows, D // 2), dtype=torch.uint8, device=dev)
+    sf = torch.empty(B.nvfp4_sf_bytes(rows, D), dtype=torch.uint8, device=dev)
+    one = torch.ones(1, device=dev)
+    y = torch.empty((rows, D), dtype=torch.float32, device=dev)
+    B.nvfp4_rmsnorm_rope_quantize(x, gamma, 1e-6, R, pos, cos_t, sin_t, one, y_out=y, codes=codes, sf=sf)
+    gs = torch.tensor([2688.0 / y.abs().max().item()], device=dev)     # calibration: the pre-computed scale
+    del y
+    stream = torch.cuda.current_stream()
+    fn = lambda: B.nvfp4_rmsnorm_rope_quantize(x, gamma, 1e-6, R, pos, cos_t, sin_t, gs, codes=codes, sf=sf)
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    if B.nvfp4moe_last_device_status() != 0:
+        raise RuntimeError("device status after warm-up")
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(1.0)
+    t0 = time.time()
+    ms, steps = _timed(stream, args.steps, fn, min_seconds=1.5)   # inputs (403 MB) exceed L2
+    clk = clocks.stop(t0, time.time())
+    per_row = 2 * D + 4 + D // 2 + D // 16
+    alg = rows * per_row
+    gbs = alg / (ms * 1e-3) / 1e9
+    peaks, kind = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    # end to end: x and positions from pinned host memory, codes and scales back
+    x_h, p_h = x.cpu().pin_memory(), pos.cpu().pin_memory()
+    c_h = torch.empty(codes.shape, dtype=torch.uint8).pin_memory()
+    s_h = torch.empty(sf.shape, dtype=torch.uint8).pin_memory()
+    x_d, p_d = torch.empty_like(x), torch.empty_like(pos)
+
+    def e2e_step():
+        x_d.copy_(x_h, non_blocking=True)
+        p_d.copy_(p_h, non_blocking=True)
+        B.nvfp4_rmsnorm_rope_quantize(x_d, gamma, 1e-6, R, p_d, cos_t, sin_t, gs, codes=codes, sf=sf)
+        c_h.copy_(codes, non_blocking=True)
+        s_h.copy_(sf, non_blocking=True)
+    e2e_step()
+    e2e_ms, _ = _timed(stream, max(3, args.steps // 10), e2e_step)
+    # CPU oracle on a bounded sample of the same rows
+    import oracle as O
+    from nvfp4_block_scaled_05_gb300 import workloads as W
+    n = 16384
+    xs = W.bf16_bits(x[:n].cpu())
+    c0 = time.perf_counter()
+    yo = O.rmsnorm_rope(xs, gamma.double().cpu().numpy(), 1e-6, R, pos[:n].cpu().numpy(),
+                        cos_t.double().cpu().numpy(), sin_t.double().cpu().numpy())
+    O.quantize_f32(yo.astype(np.float32), np.float32(gs.item()))
+    dt = time.perf_counter() - c0
+    cpu = {"value": n * per_row / dt / 1e9, "unit": "GB/s", "cores": O.get_threads(), "kind": "oracle",
+           "sample": "%d of the %d rows (norm + rope in fp64, then the f32 quantizer); %.1f s" % (n, rows, dt)}
+    line = _side_line(
+        args, "fused RMS norm + RoPE + NVFP4 quant of q-head rows, algorithmic GB/s", gbs, "GB/s", ms,
+        {"workload": "qnorm_rope", "tokens": T, "heads": H, "head_dim": D, "rope_dims": R, "rows": rows,
+         "l2": "inputs larger than L2 (403 MB of BF16 rows)", "bytes_per_row": per_row},
+        {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm, "traffic": None,
+         "kernel": "norm_rope_quantize_kernel", "kernel_ms": ms, "peak_source": kind},
+        {"value": alg / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
+         "h2d_bytes_per_step": x.numel() * 2 + pos.numel() * 4,
+         "d2h_bytes_per_step": codes.numel() + sf.numel()},
+        steps, clk, cpu, steps)
+    print(json.dumps(line), flush=True)
+
+
+def run_linear(args):
+    """The shared-expert linear (M=4096, K=7168, N=4096): dynamic-gs NVFP4
+    quantization of the BF16 activation, then nvfp4_linear to BF16."""
+    import numpy as np
+    import torch
+    from nvfp4_block_scaled_05_gb300 import binding as B
+    from nvfp4_block_scaled_05_gb300 import workloads as W
+    dev = torch.device("cuda", 0)
+    cfg = W.CONFIGS["linear"]
+    inp = W.linear_inputs(cfg, seed=args.seed, device=dev)
+    M, K, N = cfg.M, cfg.K, cfg.N
+    x = inp["x"]
+    wc, wsf, gsw = B.nvfp4_quantize(inp["w"][0])
+    a_rows = -(-M // 128) * 128
+    xc = torch.zeros((a_rows, K // 2), dtype=torch.uint8, device=dev)
+    xsf = torch.zeros(B.nvfp4_sf_bytes(a_rows, K), dtype=torch.uint8, device=dev)
+    gsx = torch.empty(1, device=dev)
+    out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    lws = torch.empty(int(B.lib().nvfp4_linear_workspace_size()), dtype=torch.uint8, device=dev)
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def fn():
+        B.nvfp4_quantize(x, codes=xc[:M], sf=xsf, gs_out=gsx)
+        B.nvfp4_linear(xc, xsf, gsx, M, wc, wsf, gsw, out=out, ws=lws)
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    if B.nvfp4moe_last_device_status() != 0:
+        raise RuntimeError("device status after warm-up")
+    stream = torch.cuda.current_stream()
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(1.0)
+    t0 = time.time()
+    ms, steps = _timed(stream, args.steps, fn, flush=lambda: flush_buf.zero_(), min_seconds=1.5)
+    clk = clocks.stop(t0, time.time())
+    flops = 2.0 * M * N * K
+    tf = flops / (ms * 1e-3) / 1e12
+    peaks, kind = load_peaks()
+    fp4 = float(peaks.get("bf16_tflops", 0)) * FP4_OVER_BF16
+    # the GEMM alone (the dominant kernel) for the roofline
+    gemm_ms, _ = _timed(stream, args.steps,
+                        lambda: B.nvfp4_linear(xc, xsf, gsx, M, wc, wsf, gsw, out=out, ws=lws),
+                        flush=lambda: flush_buf.zero_())
+    g_tf = flops / (gemm_ms * 1e-3) / 1e12
+    x_h = x.cpu().pin_memory()
+    o_h = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
+    x_d = torch.empty_like(x)
+
+    def e2e_step():
+        x_d.copy_(x_h, non_blocking=True)
+        B.nvfp4_quantize(x_d, codes=xc[:M], sf=xsf, gs_out=gsx)
+        B.nvfp4_linear(xc, xsf, gsx, M, wc, wsf, gsw, out=out, ws=lws)
+        o_h.copy_(out, non_blocking=True)
+    e2e_step()
+    e2e_ms, _ = _timed(stream, max(3, args.steps // 10), e2e_step)
+    import oracle as O
+    rows = 64
+    xb = W.bf16_bits(x[:rows].cpu())
+    c0 = time.perf_counter()
+    g1 = O.global_scale(O.amax_bf16(W.bf16_bits(x.cpu())))
+    wb = W.bf16_bits(inp["w"][0].cpu())
+    c2, s2, g2 = O.quantize_expert(wb)
+    O.matmul_nt(O.dequantize_f64(*O.quantize_bf16(xb, g1), g1), O.dequantize_f64(c2, s2, g2))
+    dt = time.perf_counter() - c0
+    cpu = {"value": 2.0 * rows * N * K / dt / 1e12, "unit": "TFLOP/s", "cores": O.get_threads(),
+           "kind": "oracle", "sample": "%d of the %d rows (activation scale over all rows, weight "
+                                       "quantization included); %.1f s" % (rows, M, dt)}
+    line = _side_line(
+        args, "shared-expert NVFP4 linear (quantize + GEMM) TFLOP/s", tf, "TFLOP/s", ms,
+        {"workload": "linear", "M": M, "K": K, "N": N,
+         "l2": "L2 flushed (256 MB written) before every timed call"},
+        {"bound": "tensor", "achieved": g_tf, "peak": fp4, "unit": "TFLOP/s", "frac": g_tf / fp4,
+         "traffic": None, "kernel": "grouped_gemm_kernel<false> (one group)", "kernel_ms": gemm_ms,
+         "peak_source": "%s bf16 burst x 6 (nominal dense fp4/bf16 ratio)" % kind},
+        {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+         "h2d_bytes_per_step": x.numel() * 2, "d2h_bytes_per_step": out.numel() * 2},
+        4 * steps, clk, cpu, steps)
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.op == "qnorm_rope":
+        return run_qnorm_rope(args)
+    if args.op == "linear":
+        return run_linear(args)
     from nvfp4_block_scaled_05_gb300 import workloads as W
     cfg = W.CONFIGS[args.workload]
     if args.impl == "reference":

@@ -248,6 +248,33 @@ int nvfp4_grouped_gemm_swiglu(const uint8_t* a_codes, const uint8_t* a_sf, const
                               int64_t K, const float* gs_h, uint8_t* h_codes, uint8_t* h_sf,
                               void* stream);
 
+/*
+ * nvfp4_rmsnorm_rope_quantize -- fused front end for attention projections
+ * (README "THE PLAN", item 3: "Q norm -> RoPE -> NVFP4 quant", all in one
+ * pass): per row of D elements
+ *   y = x / sqrt(mean(x^2) + eps) * gamma            (f32),
+ *   the last rope_dims elements rotated in adjacent pairs (2j, 2j+1) by the
+ *   angle whose cosine / sine are cos_tab / sin_tab[positions[row], j],
+ *   then y quantized to NVFP4 with the pre-computed global scale *gs.
+ *   x          (rows, D) BF16, leading dimension ldx (16-byte aligned rows).
+ *   gamma      D f32 (device, 16-byte aligned).  eps >= 0.
+ *   positions  rows int32 (device), each in [0, max_pos); a position outside
+ *              it gives that row all-zero codes and scales and records
+ *              NVFP4MOE_ERR_INVALID in the device status word.
+ *   cos_tab, sin_tab  (max_pos, rope_dims / 2) f32, row-major (device,
+ *              16-byte aligned).
+ *              With rope_dims == 0 positions and tables are not read.
+ *   codes      (rows, D/2) bytes; sf in NVFP4_SF_ROWMAJOR or NVFP4_SF_TILED.
+ *   y_out      NULL, or (rows, D) f32 that receives y (16-byte aligned).
+ * Requires D % 16 == 0, rope_dims % 16 == 0, rope_dims <= D.
+ */
+int nvfp4_rmsnorm_rope_quantize(const void* x, int64_t rows, int64_t D, int64_t ldx,
+                                const float* gamma, float eps, int64_t rope_dims,
+                                const int32_t* positions, const float* cos_tab,
+                                const float* sin_tab, int64_t max_pos, const float* gs,
+                                uint8_t* codes, uint8_t* sf, int sf_layout, float* y_out,
+                                void* stream);
+
 /* Workspace bytes nvfp4_linear needs (the row bounds of its single group). */
 size_t nvfp4_linear_workspace_size(void);
 
@@ -362,7 +389,8 @@ int moe_forward_static(const void* x, const float* router_logits, int64_t T, int
                        void* ws, size_t ws_bytes, void* stream);
 
 /* Waits for `stream`, then reads and clears the device status word that the
- * GEMM and fused-front kernels set when a bounded wait runs out (README "Key Lessons" 5: no
+ * GEMM and fused-front kernels set when a bounded wait runs out (and
+ * nvfp4_rmsnorm_rope_quantize sets on a position out of range) (README "Key Lessons" 5: no
  * silent failure). Returns NVFP4MOE_OK, NVFP4MOE_ERR_DEVICE_TIMEOUT or
  * NVFP4MOE_ERR_LAUNCH (a CUDA error on the stream). */
 int nvfp4moe_last_device_status(void* stream);

@@ -59,6 +59,9 @@ _SIGS = {
     "moe_dispatch_static": (_int, [_c_void_p, _i64, _c_void_p, _i64, _i64, _int, _int, _c_void_p, _c_void_p,
                                    _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _i64,
                                    _c_void_p, _size, _c_void_p]),
+    "nvfp4_rmsnorm_rope_quantize": (_int, [_c_void_p, _i64, _i64, _i64, _c_void_p, ctypes.c_float, _i64,
+                                           _c_void_p, _c_void_p, _c_void_p, _i64, _c_void_p, _c_void_p,
+                                           _c_void_p, _int, _c_void_p, _c_void_p]),
     "nvfp4_linear_workspace_size": (_size, []),
     "nvfp4_linear": (_int, [_c_void_p, _c_void_p, _c_void_p, _i64, _i64, _c_void_p, _c_void_p, _c_void_p,
                             _i64, _i64, _c_void_p, _i64, _c_void_p, _size, _c_void_p]),
@@ -252,6 +255,25 @@ def nvfp4_grouped_gemm(a_codes, a_sf, gs_a, b_codes, b_sf, gs_b, offsets, out=No
                                     _ptr(b_codes), _ptr(b_sf), _ptr(gs_b), _ptr(offsets), E, N, K,
                                     _ptr(out), out.stride(0), _stream()), "nvfp4_grouped_gemm")
     return out
+
+
+def nvfp4_rmsnorm_rope_quantize(x, gamma, eps, rope_dims, positions, cos_tab, sin_tab, gs,
+                                sf_layout=NVFP4_SF_TILED, y_out=None, codes=None, sf=None):
+    """(rows, D) BF16 -> RMS norm -> RoPE on the last rope_dims -> NVFP4 (codes, sf)."""
+    _dev(x, "x")
+    assert x.dtype == torch.bfloat16 and x.dim() == 2
+    rows, D = x.shape
+    dev = x.device
+    if codes is None:
+        codes = torch.empty((rows, D // 2), dtype=torch.uint8, device=dev)
+    if sf is None:
+        sf = torch.empty(nvfp4_sf_bytes(rows, D, sf_layout), dtype=torch.uint8, device=dev)
+    max_pos = cos_tab.shape[0] if cos_tab is not None else 0
+    _check(lib().nvfp4_rmsnorm_rope_quantize(_ptr(x), rows, D, x.stride(0), _ptr(gamma), float(eps), rope_dims,
+                                             _ptr(positions), _ptr(cos_tab), _ptr(sin_tab), max_pos, _ptr(gs),
+                                             _ptr(codes), _ptr(sf), sf_layout, _ptr(y_out), _stream()),
+           "nvfp4_rmsnorm_rope_quantize")
+    return codes, sf
 
 
 def nvfp4_linear(a_codes, a_sf, gs_a, M, w_codes, w_sf, gs_w, out=None, ws=None):

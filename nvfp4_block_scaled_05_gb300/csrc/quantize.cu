@@ -121,6 +121,187 @@ __global__ void __launch_bounds__(256) dispatch_quantize_kernel(
   }
 }
 
+// RMS norm -> RoPE -> NVFP4 quantization (README "THE PLAN", item 3: "Q norm
+// -> RoPE -> NVFP4 quant" in one pass).
+//
+// A row of nb = D/16 blocks is handled by a group of G lanes (G a power of two,
+// 4 <= G <= 32, the smallest with G * BPL >= nb); lane l of the group owns the
+// blocks l, l + G, ..., up to BPL of them, held in registers, so the row is
+// read once. Rows longer than 32 * BPL_MAX blocks take the second kernel
+// below, which streams the row twice. Per row: the sum of squares (per lane in
+// block order, then a butterfly over the group), y = x * (1/sqrt(mean + eps))
+// * gamma, the adjacent pairs of the rope blocks rotated with the tables at
+// the row's position, then each block quantized with the pre-computed global
+// scale. Scale bytes of 4 consecutive blocks are gathered into one 4-byte
+// store. A position outside [0, max_pos) zeroes the row's output and records
+// NVFP4MOE_ERR_INVALID in the device status word.
+struct NormRopeArgs {
+  const __nv_bfloat16* x;
+  int64_t rows, D, ldx;
+  const float* gamma;
+  float eps;
+  int64_t R;
+  const int32_t* positions;
+  const float* cos_t;
+  const float* sin_t;
+  int64_t max_pos;
+  const float* gs;
+  uint8_t* codes;
+  uint8_t* sf;
+  int sf_layout;
+  float* y_out;
+  int* status;
+};
+
+__device__ __forceinline__ void norm_rope_block(const NormRopeArgs& a, int64_t b, int64_t rope0, int32_t pos,
+                                                bool bad, float inv, float (&v)[16]) {
+  float g[16];
+  const float4* gp = reinterpret_cast<const float4*>(a.gamma + 16 * b);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 t = __ldg(gp + i);
+    g[4 * i] = t.x; g[4 * i + 1] = t.y; g[4 * i + 2] = t.z; g[4 * i + 3] = t.w;
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = v[i] * inv * g[i];
+  if (b >= rope0 && !bad) {
+    const int64_t half = a.R / 2, j0 = (b - rope0) * 8;
+    const float4* ct = reinterpret_cast<const float4*>(a.cos_t + (int64_t)pos * half + j0);
+    const float4* st = reinterpret_cast<const float4*>(a.sin_t + (int64_t)pos * half + j0);
+    const float4 c0 = __ldg(ct), c1 = __ldg(ct + 1), s0 = __ldg(st), s1 = __ldg(st + 1);
+    const float cs[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    const float sn[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float c = cs[j], s = sn[j];
+      const float x0 = v[2 * j], x1 = v[2 * j + 1];
+      v[2 * j] = x0 * c - x1 * s;
+      v[2 * j + 1] = x0 * s + x1 * c;
+    }
+  }
+  if (bad) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = 0.0f;
+  }
+}
+
+// Quantize block b of row r and store codes, y; returns the scale byte.
+__device__ __forceinline__ uint32_t norm_rope_store(const NormRopeArgs& a, int64_t r, int64_t b, float gs,
+                                                    const float (&v)[16]) {
+  uint32_t w0, w1;
+  const uint32_t sfb = quantize_block16(v, gs, w0, w1);
+  *reinterpret_cast<uint2*>(a.codes + r * (a.D / 2) + 8 * b) = make_uint2(w0, w1);
+  if (a.y_out) {
+    float4* yo = reinterpret_cast<float4*>(a.y_out + r * a.D + 16 * b);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) yo[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+  }
+  return sfb;
+}
+
+// Scale byte of block b of row r; `word` holds the bytes of blocks b..b+3 in
+// the lane whose block is a multiple of 4 (words only when the 4 bytes are
+// contiguous and aligned in the layout).
+__device__ __forceinline__ void norm_rope_store_sf(const NormRopeArgs& a, int64_t r, int64_t b, uint32_t sfb,
+                                                   uint32_t word, bool words) {
+  const int64_t nb = a.D / 16;
+  if (words) {
+    if ((b & 3) == 0) {
+      const int64_t off = a.sf_layout == NVFP4_SF_TILED ? sf_tiled_offset(r, b, (a.D + 63) / 64) : r * nb + b;
+      *reinterpret_cast<uint32_t*>(a.sf + off) = word;
+    }
+  } else {
+    const int64_t off = a.sf_layout == NVFP4_SF_TILED ? sf_tiled_offset(r, b, (a.D + 63) / 64) : r * nb + b;
+    a.sf[off] = static_cast<uint8_t>(sfb);
+  }
+}
+
+template <int G, int BPL>
+__global__ void __launch_bounds__(256) norm_rope_quantize_kernel(const NormRopeArgs a) {
+  const int lane = threadIdx.x & 31, gl = lane % G;
+  const int64_t r = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / G;
+  const unsigned gmask = G == 32 ? 0xFFFFFFFFu : (((1u << G) - 1u) << (lane - gl));
+  if (r >= a.rows) return;   // whole groups leave together (rows are per group)
+  const int64_t nb = a.D / 16, rope0 = (a.D - a.R) / 16;
+  const __nv_bfloat16* xr = a.x + r * a.ldx;
+  const int32_t pos = a.R > 0 ? a.positions[r] : 0;
+  const bool bad = a.R > 0 && (pos < 0 || pos >= a.max_pos);
+  if (bad && gl == 0 && atomicCAS(&a.status[0], 0, NVFP4MOE_ERR_INVALID) == 0) a.status[1] = 10;
+  float v[BPL][16];
+  float ss = 0.0f;
+#pragma unroll
+  for (int i = 0; i < BPL; ++i) {
+    const int64_t b = gl + (int64_t)G * i;
+    if (b < nb) {
+      const uint4* p = reinterpret_cast<const uint4*>(xr + 16 * b);
+      bf16x8_to_f32(__ldg(p), v[i]);
+      bf16x8_to_f32(__ldg(p + 1), v[i] + 8);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) ss = fmaf(v[i][e], v[i][e], ss);
+    }
+  }
+#pragma unroll
+  for (int o = G / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(gmask, ss, o);
+  const float inv = rsqrtf(ss / (float)a.D + a.eps);
+  const float gs = *a.gs;
+  // 4-byte scale words need 4 consecutive blocks in 4 consecutive lanes
+  const bool words = (nb % 4) == 0 && G >= 4;
+#pragma unroll
+  for (int i = 0; i < BPL; ++i) {
+    const int64_t b = gl + (int64_t)G * i;
+    uint32_t sfb = 0;
+    if (b < nb) {
+      norm_rope_block(a, b, rope0, pos, bad, inv, v[i]);
+      sfb = norm_rope_store(a, r, b, gs, v[i]);
+    }
+    const uint32_t b1 = __shfl_down_sync(gmask, sfb, 1, G);
+    const uint32_t b2 = __shfl_down_sync(gmask, sfb, 2, G);
+    const uint32_t b3 = __shfl_down_sync(gmask, sfb, 3, G);
+    if (b < nb) norm_rope_store_sf(a, r, b, sfb, sfb | (b1 << 8) | (b2 << 16) | (b3 << 24), words);
+  }
+}
+
+// Long rows: one warp per row, the row streamed twice (sum of squares, then
+// the rest); scale bytes stored one by one.
+__global__ void __launch_bounds__(256) norm_rope_quantize_long_kernel(const NormRopeArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int64_t r = blockIdx.x * (int64_t)(blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (r >= a.rows) return;
+  const int64_t nb = a.D / 16, rope0 = (a.D - a.R) / 16;
+  const __nv_bfloat16* xr = a.x + r * a.ldx;
+  const int32_t pos = a.R > 0 ? a.positions[r] : 0;
+  const bool bad = a.R > 0 && (pos < 0 || pos >= a.max_pos);
+  if (bad && lane == 0 && atomicCAS(&a.status[0], 0, NVFP4MOE_ERR_INVALID) == 0) a.status[1] = 10;
+  float ss = 0.0f;
+  for (int64_t b = lane; b < nb; b += 32) {
+    float v[16];
+    const uint4* p = reinterpret_cast<const uint4*>(xr + 16 * b);
+    bf16x8_to_f32(__ldg(p), v);
+    bf16x8_to_f32(__ldg(p + 1), v + 8);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) ss = fmaf(v[i], v[i], ss);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+  const float inv = rsqrtf(ss / (float)a.D + a.eps);
+  const float gs = *a.gs;
+  for (int64_t b = lane; b < nb; b += 32) {
+    float v[16];
+    const uint4* p = reinterpret_cast<const uint4*>(xr + 16 * b);
+    bf16x8_to_f32(__ldg(p), v);
+    bf16x8_to_f32(__ldg(p + 1), v + 8);
+    norm_rope_block(a, b, rope0, pos, bad, inv, v);
+    const uint32_t sfb = norm_rope_store(a, r, b, gs, v);
+    norm_rope_store_sf(a, r, b, sfb, 0u, false);
+  }
+}
+
+template <int G, int BPL>
+void launch_norm_rope(const NormRopeArgs& a, cudaStream_t s) {
+  const int64_t threads = a.rows * G;
+  norm_rope_quantize_kernel<G, BPL><<<(unsigned)ceil_div(threads, 256), 256, 0, s>>>(a);
+}
+
 int launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ldx, const int32_t* row_src,
                 uint32_t* amax_bits, cudaStream_t s) {
   if (cudaMemsetAsync(amax_bits, 0, sizeof(uint32_t), s) != cudaSuccess) return NVFP4MOE_ERR_LAUNCH;
@@ -197,5 +378,38 @@ extern "C" int moe_quantize_dispatch(const void* x, int64_t T, int64_t K, int64_
   dispatch_quantize_kernel<<<(unsigned)ceil_div(warps, kWarpsPerBlock), 256, 0, s>>>(
       static_cast<const __nv_bfloat16*>(x), T, K, ldx, k, gs_in, gs_in ? nullptr : amax_bits,
       gs_out, topk_ids, offsets, flat_to_perm, pad_off, a_codes, a_sf);
+  return launch_status();
+}
+
+extern "C" int nvfp4_rmsnorm_rope_quantize(const void* x, int64_t rows, int64_t D, int64_t ldx,
+                                           const float* gamma, float eps, int64_t rope_dims,
+                                           const int32_t* positions, const float* cos_tab,
+                                           const float* sin_tab, int64_t max_pos, const float* gs,
+                                           uint8_t* codes, uint8_t* sf, int sf_layout, float* y_out,
+                                           void* stream) {
+  NVFP4_CHECK(rows >= 0 && D > 0 && D % 16 == 0 && rope_dims >= 0 && rope_dims % 16 == 0 && rope_dims <= D,
+              NVFP4MOE_ERR_UNSUPPORTED);
+  NVFP4_CHECK(sf_layout == NVFP4_SF_ROWMAJOR || sf_layout == NVFP4_SF_TILED, NVFP4MOE_ERR_INVALID);
+  if (rows == 0) return NVFP4MOE_OK;
+  NVFP4_CHECK(x && gamma && gs && codes && sf && eps >= 0.0f, NVFP4MOE_ERR_INVALID);
+  NVFP4_CHECK(rope_dims == 0 || (positions && cos_tab && sin_tab && max_pos > 0), NVFP4MOE_ERR_INVALID);
+  NVFP4_CHECK(ldx >= D && ldx % 8 == 0 && aligned(x, 16) && aligned(codes, 8) && aligned(sf, 4) &&
+                  aligned(gamma, 16) && (!y_out || aligned(y_out, 16)) &&
+                  (rope_dims == 0 || (aligned(cos_tab, 16) && aligned(sin_tab, 16))),
+              NVFP4MOE_ERR_INVALID);
+  NVFP4_CHECK(rows * 32 < (1ll << 40), NVFP4MOE_ERR_UNSUPPORTED);
+  int* status = device_status_word();
+  NVFP4_CHECK(status, NVFP4MOE_ERR_LAUNCH);
+  NormRopeArgs a{static_cast<const __nv_bfloat16*>(x), rows, D, ldx, gamma, eps, rope_dims, positions,
+                 cos_tab, sin_tab, max_pos, gs, codes, sf, sf_layout, y_out, status};
+  cudaStream_t s = as_stream(stream);
+  const int64_t nb = D / 16;
+  if (nb <= 4) launch_norm_rope<4, 1>(a, s);
+  else if (nb <= 8) launch_norm_rope<8, 1>(a, s);
+  else if (nb <= 16) launch_norm_rope<16, 1>(a, s);
+  else if (nb <= 32) launch_norm_rope<32, 1>(a, s);
+  else if (nb <= 64) launch_norm_rope<32, 2>(a, s);
+  else if (nb <= 128) launch_norm_rope<32, 4>(a, s);
+  else norm_rope_quantize_long_kernel<<<(unsigned)ceil_div(rows, 8), 256, 0, s>>>(a);
   return launch_status();
 }

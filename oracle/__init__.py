@@ -60,6 +60,8 @@ def lib():
                                         _i64, _i64, ctypes.c_int, _f64p]),
             "orc_swiglu": (None, [_f64p, _i64, _i64, _f32p]),
             "orc_combine": (None, [_f64p, _i64, _f64p, _i32p, _i64, ctypes.c_int, _f64p]),
+            "orc_rmsnorm_rope": (None, [_u16p, _i64, _i64, _i64, _f64p, ctypes.c_double, _i64, _i32p,
+                                        _f64p, _f64p, _f64p]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -240,6 +242,24 @@ def combine(out: np.ndarray, w: np.ndarray, flat_to_perm: np.ndarray) -> np.ndar
     K = out.shape[1]
     y = np.zeros((T, K), np.float64)
     lib().orc_combine(out, K, w, _c(flat_to_perm, np.int32), T, k, y)
+    return y
+
+
+def rmsnorm_rope(x, gamma, eps, rope_dims, positions, cos_t, sin_t) -> np.ndarray:
+    """README "THE PLAN", item 3 ("Q norm -> RoPE -> NVFP4 quant", one pass),
+    the norm and rotation steps, in fp64: y = x / sqrt(mean(x^2) + eps) * gamma
+    per row, then adjacent pairs of the last ``rope_dims`` elements rotated by
+    the angle whose cosine / sine are ``cos_t[pos, j]`` / ``sin_t[pos, j]``.
+    x: (rows, D) BF16 bits; gamma (D,); positions (rows,) int; tables
+    (max_pos, rope_dims/2). Returns (rows, D) fp64."""
+    x = _c(x, np.uint16)
+    rows, D = x.shape
+    y = np.zeros((rows, D), np.float64)
+    half = rope_dims // 2
+    ct = _c(np.asarray(cos_t, np.float64).reshape(-1, max(half, 1)), np.float64)
+    st = _c(np.asarray(sin_t, np.float64).reshape(-1, max(half, 1)), np.float64)
+    lib().orc_rmsnorm_rope(x, rows, D, D, _c(gamma, np.float64), float(eps), rope_dims,
+                           _c(positions, np.int32), ct, st, y)
     return y
 
 

@@ -38,6 +38,13 @@
 //   R6 permutation: rows of one expert are ordered by ascending flat slot
 //      f = t*k + j (stable counting sort).
 //   R7 dequantized value = code * s / gs; GEMMs accumulate in fp64.
+//   R13 RMS norm (README "THE PLAN", item 3: "Q norm -> RoPE -> NVFP4 quant" in
+//      one pass): y_i = x_i / sqrt(mean_i(x_i^2) + eps) * gamma_i over the D
+//      elements of a row, in fp64.
+//   R14 RoPE on the last R elements of the row: adjacent pairs (2j, 2j+1)
+//      counted from the first rope element are rotated by the angle whose
+//      cosine and sine are the caller's tables at [position][j]; the first
+//      D - R elements are left as normed.
 
 #include <cmath>
 #include <cstdint>
@@ -148,6 +155,8 @@ static void parallel_rows(int64_t rows, F fn) {
 
 extern "C" {
 
+static inline float bf16_to_f32(uint16_t b);
+static inline double bf16_to_double(uint16_t b) { return (double)bf16_to_f32(b); }
 static inline float bf16_to_f32(uint16_t b) {
   uint32_t u = (uint32_t)b << 16;
   float f;
@@ -367,6 +376,31 @@ void orc_combine(const double* out, int64_t K, const double* w, const int32_t* f
       for (int j = 0; j < k; ++j) acc += w[t * k + j] * out[(int64_t)flat_to_perm[t * k + j] * K + c];
       y[t * K + c] = acc;
     }
+}
+
+// R13 + R14: RMS norm, then rotary embedding of the last R elements.
+// x: rows x D BF16 bits (leading dimension ldx); gamma[D]; pos[rows];
+// cos_t / sin_t: (max_pos x R/2), row-major; y: rows x D fp64.
+void orc_rmsnorm_rope(const uint16_t* x, int64_t rows, int64_t D, int64_t ldx, const double* gamma,
+                      double eps, int64_t R, const int32_t* pos, const double* cos_t,
+                      const double* sin_t, double* y) {
+  for (int64_t r = 0; r < rows; ++r) {
+    double ss = 0.0;
+    for (int64_t i = 0; i < D; ++i) {
+      const double v = bf16_to_double(x[r * ldx + i]);
+      ss += v * v;
+    }
+    const double inv = 1.0 / std::sqrt(ss / (double)D + eps);
+    double* yr = y + r * D;
+    for (int64_t i = 0; i < D; ++i) yr[i] = bf16_to_double(x[r * ldx + i]) * inv * gamma[i];
+    const int64_t s0 = D - R;
+    for (int64_t j = 0; j < R / 2; ++j) {
+      const double c = cos_t[(int64_t)pos[r] * (R / 2) + j], s = sin_t[(int64_t)pos[r] * (R / 2) + j];
+      const double a = yr[s0 + 2 * j], b = yr[s0 + 2 * j + 1];
+      yr[s0 + 2 * j] = a * c - b * s;
+      yr[s0 + 2 * j + 1] = a * s + b * c;
+    }
+  }
 }
 
 }  // extern "C"

@@ -15,10 +15,14 @@
 // it feeds, so four warps write them with tcgen05.st instead, each into its
 // own TMEM lane quadrant, in parallel.
 // Warp roles (448 threads, one CTA per SM):
-//   warp 0      TMA producer: A and B code tiles (tiled TMA, 128B swizzle) and
-//               their scale atoms (bulk copies) into a 4-stage ring
+//   warp 0      TMA producer: A and B code tiles (tiled TMA, 128B swizzle)
+//               into a 4-stage ring
 //   warp 1      TMEM owner; one lane issues the MMAs
-//   warps 2-5   scale warps, one per TMEM lane quadrant q: per K=64 step the A
+//   warps 2-5   scale warps, one per TMEM lane quadrant q. The scale atoms
+//               reach a shared-memory ring either by the producer's bulk
+//               copies (L1) or by the scale warps' own cp.async copies up to 4
+//               stages ahead (L2: the load path adds to the TMA engine's
+//               bandwidth, which the code tiles saturate). Per K=64 step the A
 //               scale of each of the quadrant's 32 rows goes to column 4kk+q
 //               (the MMA reads quadrant q's A scales from column base+q), and
 //               the 256 B-row scales to columns 8kk..8kk+7 (B scales are read
@@ -54,11 +58,11 @@ constexpr int kThreads = 32 * (2 + kScaleWarps + kEpiWarps);
 constexpr int A_BYTES = BM * BK / 2;          // 16 KB
 constexpr int B_BYTES = BN * BK / 2;          // 32 KB
 constexpr int SFA_BYTES = 4 * 512;            // 4 scale atoms (K=256) of 128 rows
-constexpr int SFB_BYTES = 2 * SFA_BYTES;      // two 128-row halves of B
+constexpr int SF_BYTES = 3 * SFA_BYTES;       // SFA, then SFB's two 128-row halves
 constexpr int OFF_B = STAGES * A_BYTES;
-constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
-constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
-constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
+constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
+constexpr int OFF_BAR = OFF_SF + STAGES * SF_BYTES;
+constexpr int kScaleThreads = 32 * 4;         // the scale warps
 constexpr int OFF_MISC = OFF_BAR + 256;
 constexpr int OFF_SCHED = OFF_MISC + 256;
 constexpr uint32_t TMEM_COLS = 512;
@@ -176,7 +180,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_acce = bar_accf + 8;
   const uint32_t bar_aux = bar_acce + 8;                   // MMA drain on abort
   const uint32_t bar_never = bar_aux + 8;                  // never arrived on (failure-path test)
-  const uint32_t bar_sffull = bar_never + 8;               // STAGES x 8 bytes: scale atoms landed
+  const uint32_t bar_sfland = bar_never + 8;               // STAGES: a stage's scale atoms landed
+  const uint32_t bar_sfcons = bar_sfland + STAGES * 8;     // STAGES: its scale atoms read by all scale warps
+  const uint32_t bar_sffull = bar_sfcons + STAGES * 8;     // STAGES: scale atoms copied by the producer landed
+  // Scale atoms reach shared memory either as bulk copies from the TMA
+  // producer (L1: its epilogue's register spills use the load path) or as
+  // cp.async copies from the scale warps (L2), whose load path adds to the
+  // TMA engine's bandwidth.
+  constexpr bool kScalesByTMA = kSwiGLU;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
   int32_t* tile_start = reinterpret_cast<int32_t*>(smem + OFF_SCHED);
@@ -209,8 +220,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 32) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_sffull + 8 * s, 1);
       mbar_init(bar_sfready + 8 * s, kScaleWarps);
+      mbar_init(bar_sfland + 8 * s, kScaleThreads);
+      mbar_init(bar_sfcons + 8 * s, kScaleWarps);
+      mbar_init(bar_sffull + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
     }
     mbar_init(bar_accf, 1);
@@ -270,20 +283,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool has_next = t + (int)gridDim.x < total;
       if (has_next) nxt = tile_src(t + gridDim.x);
       for (int kb = 0; kb < kblocks; ++kb) {
-        const int nk = min(4, ksteps - kb * 4);
         if (!wait_bounded(bar_empty + 8 * stage, phase ^ 1, abort_flag, p.wait_limit_ns, p.status, 1)) {
           ok = false;
           break;
         }
-        // codes and scales complete on separate barriers: the scale warps start
-        // as soon as the (small) scale atoms land
+        if constexpr (kScalesByTMA) {
+          const int nk = min(4, ksteps - kb * 4);
+          const uint32_t sffull = bar_sffull + 8 * stage;
+          const uint32_t sdst = sbase + OFF_SF + stage * SF_BYTES;
+          mbar_arrive_expect_tx(sffull, (1 + cur.bhalves) * nk * 512);
+          bulk_load(sdst, cur.sfa + kb * 2048, nk * 512, sffull, pol_a);
+          for (int h = 0; h < cur.bhalves; ++h)
+            bulk_load(sdst + SFA_BYTES + h * SFA_BYTES, cur.sfb + h * p.sf_rowtile_bytes + kb * 2048, nk * 512,
+                      sffull, pol_w);
+        }
         const uint32_t full = bar_full + 8 * stage;
-        const uint32_t sffull = bar_sffull + 8 * stage;
-        mbar_arrive_expect_tx(sffull, (1 + cur.bhalves) * nk * 512);
-        bulk_load(sbase + OFF_SFA + stage * SFA_BYTES, cur.sfa + kb * 2048, nk * 512, sffull, pol_a);
-        for (int h = 0; h < cur.bhalves; ++h)
-          bulk_load(sbase + OFF_SFB + stage * SFB_BYTES + h * SFA_BYTES,
-                    cur.sfb + h * p.sf_rowtile_bytes + kb * 2048, nk * 512, sffull, pol_w);
         // the B box always moves 256 rows; rows past this expert's last weight
         // tile are never multiplied (N=128 MMA), rows past the tensor read zeros
         mbar_arrive_expect_tx(full, cur.box * 128 + BN * 128);
@@ -303,51 +317,109 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < STAGES; ++s)
         if ((filled >> s) & 1u) {
           drain_wait(bar_full + 8 * s, (fill_phase >> s) & 1u);
-          drain_wait(bar_sffull + 8 * s, (fill_phase >> s) & 1u);
+          if constexpr (kScalesByTMA) drain_wait(bar_sffull + 8 * s, (fill_phase >> s) & 1u);
         }
   } else if (warp >= 2 && warp < kFirstEpiWarp) {
     // ---------------------------------------------------------------- scale warps
+    // The scale atoms travel through the load path (cp.async), not the TMA
+    // engine that the code tiles saturate: the 128 scale threads copy a stage's
+    // atoms (up to 6 KB) into a 4-slot shared-memory ring up to STAGES stages
+    // ahead; a slot is refilled once all four warps have read it. Per stage,
+    // each warp then stores its quadrant's scales into the stage's TMEM slot.
     const int q = warp & 3;                               // TMEM lane quadrant of this warp
     const uint32_t lanes = static_cast<uint32_t>(q * 32) << 16;
-    uint32_t stage = 0, phase = 0;
+    const int st_id = (warp - 2) * 32 + lane;              // 0..127 among the scale threads
+    const int my_tiles = blockIdx.x < total ? (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int nstages = my_tiles * kblocks;
+    // copy cursor: tile, k-block and the tile's scale sources
+    int ct = blockIdx.x, ckb = 0;
+    const uint8_t* csfa = nullptr;
+    const uint8_t* csfb = nullptr;
+    bool ctwo = false;
+    auto load_tile = [&](int t) {
+      int e, nb, mb, rows, ncols;
+      sch.decode(t, e, nb, mb, rows, ncols);
+      csfa = p.a_sf + (int64_t)((pad_off[e] + mb * BM) / BM) * p.sf_rowtile_bytes;
+      csfb = p.b_sf + (int64_t)e * p.b_sf_expert_bytes + (int64_t)(nb * 2) * p.sf_rowtile_bytes;
+      ctwo = ncols > 128;
+    };
+    if (!kScalesByTMA && nstages > 0) load_tile(ct);
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-      for (int kb = 0; kb < kblocks; ++kb) {
-        // every lane waits, then the warp agrees (the stores below are warp-wide)
-        ok = wait_bounded(bar_sffull + 8 * stage, phase, abort_flag, p.wait_limit_ns, p.status, 5);
-        ok = __all_sync(0xFFFFFFFFu, ok);
-        if (!ok) break;
-        // Atom layout: 16-byte chunk `lane` of a 512-byte atom holds rows lane,
-        // lane+32, lane+64, lane+96 (4 bytes each, one per 16-element block).
-        // Every k-step slot is written, also past the last one of a K tail: the
-        // MMAs never read those columns, and the stale bytes stay in bounds.
-        const uint8_t* ssfa = smem + OFF_SFA + stage * SFA_BYTES + lane * 16 + q * 4;
-        const uint8_t* ssfb = smem + OFF_SFB + stage * SFB_BYTES + lane * 16;
-        uint32_t a[4], b[32];
+    int gc = 0;                                           // next stage to copy
+    auto issue = [&]() -> bool {
+      if constexpr (kScalesByTMA) return true;           // the producer copies the atoms
+      const int slot = gc % STAGES, use = gc / STAGES;
+      if (use > 0 && !wait_bounded(bar_sfcons + 8 * slot, (use - 1) & 1, abort_flag, p.wait_limit_ns, p.status, 5))
+        return false;
+      const int nk = min(4, ksteps - ckb * 4);
+      const uint32_t dst = sbase + OFF_SF + slot * SF_BYTES;
+      // 384 chunks of 16 bytes: SFA atoms (128), then SFB halves 0 and 1 (128 each);
+      // chunks past a K tail, or of a missing second half, are not copied
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          a[kk] = *reinterpret_cast<const uint32_t*>(ssfa + kk * 512);    // row 32q + lane
-          // B rows lane+32j, j = 0..3 (first 128 rows) and 4..7 (second 128 rows);
-          // for a 128-column tile the second half is stale and never read
-          const uint4 lo = *reinterpret_cast<const uint4*>(ssfb + kk * 512);
-          const uint4 hi = *reinterpret_cast<const uint4*>(ssfb + SFA_BYTES + kk * 512);
-          b[8 * kk + 0] = lo.x; b[8 * kk + 1] = lo.y; b[8 * kk + 2] = lo.z; b[8 * kk + 3] = lo.w;
-          b[8 * kk + 4] = hi.x; b[8 * kk + 5] = hi.y; b[8 * kk + 6] = hi.z; b[8 * kk + 7] = hi.w;
-        }
-        const uint32_t sfa_t = tmem + lanes + SFA_TMEM0 + stage * SFA_SLOT + q;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) tc_st1(sfa_t + 4 * kk, a[kk]);
-        tc_st32(tmem + lanes + SFB_TMEM0 + stage * SFB_SLOT, b);
-        tc_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_sfready + 8 * stage);
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1;
+      for (int i = 0; i < 3; ++i) {
+        const int c = st_id + kScaleThreads * i;           // region i, chunk st_id
+        const bool live = st_id < nk * 32 && (i < 2 || ctwo);
+        if (live) {
+          const uint8_t* src = i == 0 ? csfa + ckb * 2048 + st_id * 16
+                                      : csfb + (int64_t)(i - 1) * p.sf_rowtile_bytes + ckb * 2048 + st_id * 16;
+          cp_async_16(dst + c * 16, src);
         }
       }
+      cp_async_arrive_noinc(bar_sfland + 8 * slot);
+      ++gc;
+      if (++ckb == kblocks) {
+        ckb = 0;
+        ct += gridDim.x;
+        if (ct < total) load_tile(ct);
+      }
+      return true;
+    };
+    for (int g = 0; ok && g < nstages; ++g) {
+      if constexpr (!kScalesByTMA) {
+        while (ok && gc < nstages && gc < g + STAGES) ok = __all_sync(0xFFFFFFFFu, issue());
+        if (!ok) break;
+      }
+      const int slot = g % STAGES, use = g / STAGES;
+      ok = wait_bounded((kScalesByTMA ? bar_sffull : bar_sfland) + 8 * slot, use & 1, abort_flag,
+                        p.wait_limit_ns, p.status, 5);
+      ok = __all_sync(0xFFFFFFFFu, ok);
+      if (!ok) break;
+      // Atom layout: 16-byte chunk `lane` of a 512-byte atom holds rows lane,
+      // lane+32, lane+64, lane+96 (4 bytes each, one per 16-element block); the
+      // word of row 32q + lane is word q. Slots past a K tail (and the second
+      // half of a 128-column tile) hold stale bytes the MMAs never read.
+      const uint8_t* ssfa = smem + OFF_SF + slot * SF_BYTES + lane * 16 + q * 4;
+      const uint8_t* ssfb = smem + OFF_SF + slot * SF_BYTES + SFA_BYTES + lane * 16;
+      uint32_t a[4], b[32];
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        a[kk] = *reinterpret_cast<const uint32_t*>(ssfa + kk * 512);    // row 32q + lane
+        // B rows lane+32j, j = 0..3 (first 128 rows) and 4..7 (second 128 rows)
+        const uint4 lo = *reinterpret_cast<const uint4*>(ssfb + kk * 512);
+        const uint4 hi = *reinterpret_cast<const uint4*>(ssfb + SFA_BYTES + kk * 512);
+        b[8 * kk + 0] = lo.x; b[8 * kk + 1] = lo.y; b[8 * kk + 2] = lo.z; b[8 * kk + 3] = lo.w;
+        b[8 * kk + 4] = hi.x; b[8 * kk + 5] = hi.y; b[8 * kk + 6] = hi.z; b[8 * kk + 7] = hi.w;
+      }
+      __syncwarp();
+      if constexpr (!kScalesByTMA) {
+        if (lane == 0) mbar_arrive(bar_sfcons + 8 * slot);
+        // the TMEM slot is free once the MMAs of its previous use completed
+        // (with producer copies, their landing already implies it)
+        ok = wait_bounded(bar_empty + 8 * slot, (use & 1) ^ 1, abort_flag, p.wait_limit_ns, p.status, 5);
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        if (!ok) break;
+      }
+      const uint32_t sfa_t = tmem + lanes + SFA_TMEM0 + slot * SFA_SLOT + q;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) tc_st1(sfa_t + 4 * kk, a[kk]);
+      tc_st32(tmem + lanes + SFB_TMEM0 + slot * SFB_SLOT, b);
+      tc_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_sfready + 8 * slot);
     }
+    // this thread's copies land before the CTA may exit
+    cp_async_wait_all();
   } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------------------- MMA issuer
     uint32_t stage = 0, phase = 0, aphase = 0;

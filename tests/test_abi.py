@@ -73,3 +73,58 @@ def test_invalid_arguments_are_rejected_on_the_host(lib):
     assert st == -2
     lib.moe_forward_workspace_size.restype = ctypes.c_size_t
     assert lib.moe_forward_workspace_size(ctypes.c_int64(8), ctypes.c_int64(100), ctypes.c_int64(64), 8, 2) == 0
+
+
+def test_host_fault_injection_rejected_before_any_launch(lib):
+    """Too-small workspaces, null and misaligned pointers and unsupported shapes
+    come back as status codes from the host checks, before anything is
+    launched (no GPU needed)."""
+    vp, i64, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
+    for name in ["moe_forward", "moe_forward_static", "nvfp4_linear", "nvfp4_rmsnorm_rope_quantize",
+                 "moe_dispatch_static", "moe_permute", "moe_combine"]:
+        getattr(lib, name).restype = ctypes.c_int
+    lib.moe_forward_workspace_size.restype = ctypes.c_size_t
+    T, K, I, E, k = 16, 256, 128, 8, 2
+    need = lib.moe_forward_workspace_size(i64(T), i64(K), i64(I), E, k)
+    assert need > 0
+    p = vp(1 << 20)
+    # workspace one byte short / misaligned / absent
+    args = [p, p, i64(T), i64(K), i64(I), E, k, p, p, p, p, p, p, p, p]
+    assert lib.moe_forward(*args, p, sz(need - 1), None) == -3
+    assert lib.moe_forward(*args, vp((1 << 20) + 16), sz(need), None) == -3
+    assert lib.moe_forward(*args, None, sz(need), None) == -3
+    # a null weight pointer
+    bad = list(args)
+    bad[7] = None
+    assert lib.moe_forward(*bad, p, sz(need), None) == -1
+    # unsupported shapes: K not a multiple of 128, k > E
+    assert lib.moe_forward(p, p, i64(T), i64(200), i64(I), E, k, p, p, p, p, p, p, p, p, p, sz(need), None) == -2
+    assert lib.moe_forward(p, p, i64(T), i64(K), i64(I), 4, 5, p, p, p, p, p, p, p, p, p, sz(need), None) == -2
+    # the static forward needs its pre-computed gs_x
+    assert lib.moe_forward_static(p, p, i64(T), i64(K), i64(I), E, k, None, p, p, p, p, p, p, p, p, p, sz(need),
+                                  None) == -1
+    # static dispatch: padded operand too small
+    lib.moe_dispatch_static_workspace_size.restype = ctypes.c_size_t
+    wsd = lib.moe_dispatch_static_workspace_size(i64(T), E)
+    assert wsd > 0
+    assert lib.moe_dispatch_static(p, i64(K), p, i64(T), i64(K), E, k, p, p, p, p, p, p, p, p, i64(128), p, sz(wsd),
+                                   None) == -1
+    # linear: row capacity below 128 * ceil(M / 128); workspace too small
+    lib.nvfp4_linear_workspace_size.restype = ctypes.c_size_t
+    lws = lib.nvfp4_linear_workspace_size()
+    assert lib.nvfp4_linear(p, p, p, i64(130), i64(128), p, p, p, i64(256), i64(256), p, i64(256), p, sz(lws),
+                            None) == -1
+    assert lib.nvfp4_linear(p, p, p, i64(100), i64(128), p, p, p, i64(256), i64(256), p, i64(256), p,
+                            sz(lws - 1), None) == -3
+    # norm + rope + quant: rope_dims not a multiple of 16, missing tables, misaligned gamma
+    f = ctypes.c_float
+    assert lib.nvfp4_rmsnorm_rope_quantize(p, i64(4), i64(192), i64(192), p, f(1e-6), i64(40), p, p, p, i64(10),
+                                           p, p, p, 1, None, None) == -2
+    assert lib.nvfp4_rmsnorm_rope_quantize(p, i64(4), i64(192), i64(192), p, f(1e-6), i64(64), None, p, p,
+                                           i64(10), p, p, p, 1, None, None) == -1
+    assert lib.nvfp4_rmsnorm_rope_quantize(p, i64(4), i64(192), i64(192), vp((1 << 20) + 4), f(1e-6), i64(64), p,
+                                           p, p, i64(10), p, p, p, 1, None, None) == -1
+    # permute: workspace too small
+    lib.moe_permute_workspace_size.restype = ctypes.c_size_t
+    pws = lib.moe_permute_workspace_size(i64(T), k, E)
+    assert lib.moe_permute(p, i64(T), k, E, p, p, p, p, sz(pws - 1), None) == -3

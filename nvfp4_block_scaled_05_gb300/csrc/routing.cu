@@ -122,6 +122,8 @@ __global__ void __launch_bounds__(32) perm_scatter_kernel(const int32_t* __restr
   }
 }
 
+constexpr int kCombineCols = 1024;   // columns per block: 128 threads x 8
+
 __global__ void __launch_bounds__(128) combine_kernel(const __nv_bfloat16* __restrict__ out,
                                                       int64_t ldo, const float* __restrict__ w,
                                                       const int32_t* __restrict__ flat_to_perm,
@@ -129,13 +131,15 @@ __global__ void __launch_bounds__(128) combine_kernel(const __nv_bfloat16* __res
                                                       __nv_bfloat16* __restrict__ y, int64_t ldy) {
   __shared__ int64_t row[16];
   __shared__ float wt[16];
+  // block (t, part): token t, columns [part * kCombineCols, (part + 1) * kCombineCols)
   const int64_t t = blockIdx.x;
   if (threadIdx.x < k) {
     row[threadIdx.x] = flat_to_perm[t * k + threadIdx.x];
     wt[threadIdx.x] = w[t * k + threadIdx.x];
   }
   __syncthreads();
-  for (int64_t c = threadIdx.x * 8; c < K; c += blockDim.x * 8) {
+  const int64_t c_end = min(K, (int64_t)(blockIdx.y + 1) * kCombineCols);
+  for (int64_t c = (int64_t)blockIdx.y * kCombineCols + threadIdx.x * 8; c < c_end; c += blockDim.x * 8) {
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
@@ -216,8 +220,8 @@ extern "C" int moe_combine(const void* out, int64_t ldo, const float* topk_w,
   NVFP4_CHECK(ldo >= K && ldy >= K && ldo % 8 == 0 && ldy % 8 == 0 && aligned(out, 16) &&
                   aligned(y, 16),
               NVFP4MOE_ERR_INVALID);
-  NVFP4_CHECK(T < (1ll << 31), NVFP4MOE_ERR_UNSUPPORTED);
-  combine_kernel<<<(unsigned)T, 128, 0, as_stream(stream)>>>(
+  NVFP4_CHECK(T < (1ll << 31) && ceil_div(K, kCombineCols) <= 65535, NVFP4MOE_ERR_UNSUPPORTED);
+  combine_kernel<<<dim3((unsigned)T, (unsigned)ceil_div(K, kCombineCols)), 128, 0, as_stream(stream)>>>(
       static_cast<const __nv_bfloat16*>(out), ldo, topk_w, flat_to_perm, k, K,
       static_cast<__nv_bfloat16*>(y), ldy);
   return launch_status();

@@ -10,8 +10,8 @@
 //            their experts -> counts[c][e]
 //   -- grid barrier --
 //   phase 2  block c turns the columns e = c, c+G, ... into exclusive prefixes
-//            over blocks (counts[c'][e] = slots of expert e in blocks < c')
-//            and writes the column total
+//            over blocks (counts[c'][e] = slots of expert e in blocks < c'),
+//            one block-wide scan per column, and writes the column total
 //   -- grid barrier --
 //   phase 3  every block: exclusive scans of the totals -> offsets (block 0
 //            writes them) and padded group starts; the stable position of
@@ -124,6 +124,7 @@ __global__ void __launch_bounds__(kFrontThreads) moe_front_kernel(const FrontPar
   int32_t* slot_e = pad + (E + 1);       // [tpb * k]
   int32_t* slot_pos = slot_e + p.tpb * k;
   int32_t* misc = slot_pos + p.tpb * k;  // [32]: warp totals, barrier flag
+  int32_t* col = misc + 32;              // [G]: one expert's counts over the blocks
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = kFrontThreads / 32;
   const int G = gridDim.x, c = blockIdx.x;
   const int64_t t0 = (int64_t)c * p.tpb;
@@ -155,21 +156,14 @@ __global__ void __launch_bounds__(kFrontThreads) moe_front_kernel(const FrontPar
   if (!grid_barrier(p, (unsigned)G, 8, misc + 31)) return;
 
   // ---- phase 2: per expert column, exclusive prefix over blocks and total
-  for (int e = c + G * warp; e < E; e += G * nwarps) {
-    int carry = 0;
-    for (int base = 0; base < G; base += 32) {
-      const int cc = base + lane;
-      const int v = cc < G ? __ldcg(p.counts + (int64_t)cc * E + e) : 0;
-      int incl = v;
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, d);
-        if (lane >= d) incl += y;
-      }
-      if (cc < G) p.counts[(int64_t)cc * E + e] = carry + incl - v;
-      carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
-    }
-    if (lane == 0) p.totals[e] = carry;
+  for (int e = c; e < E; e += G) {
+    for (int cc = tid; cc < G; cc += kFrontThreads) col[cc] = __ldcg(p.counts + (int64_t)cc * E + e);
+    __syncthreads();
+    const int last = tid == 0 ? col[G - 1] : 0;     // the scan reads before it writes
+    block_exclusive_scan(col, G, misc);
+    for (int cc = tid; cc < G; cc += kFrontThreads) p.counts[(int64_t)cc * E + e] = col[cc];
+    if (tid == 0) p.totals[e] = col[G - 1] + last;
+    __syncthreads();
   }
   if (!grid_barrier(p, 2u * G, 9, misc + 31)) return;
 
@@ -229,7 +223,7 @@ __global__ void __launch_bounds__(kFrontThreads) moe_front_kernel(const FrontPar
   }
 }
 
-size_t front_smem_bytes(int E, int slots) { return (size_t)(3 * E + 2 + 2 * slots + 32) * 4; }
+size_t front_smem_bytes(int E, int slots) { return (size_t)(3 * E + 2 + 2 * slots + 32 + kFrontMaxBlocks) * 4; }
 
 template <int VPL>
 int launch_front_vpl(FrontParams& p, int G, size_t smem, cudaStream_t s) {

@@ -107,14 +107,19 @@ __global__ void __launch_bounds__(256) dispatch_quantize_kernel(
   if (t >= T) return;
   const int64_t col0 = (gw - t * nchunk) * kChunk + lane * 16;
   const bool valid = col0 < K;
+  // lane j < k finds the padded row of slot j while the row is being quantized
+  int my_prow = 0;
+  if (lane < k) {
+    const int64_t f = t * k + lane;
+    const int e = topk_ids[f];
+    my_prow = pad_off[e] + flat_to_perm[f] - offsets[e];
+  }
   uint32_t w0 = 0, w1 = 0, s = 0;
   if (valid) s = quantize_lane16(x + t * ldx, col0, gs, w0, w1);
   const uint32_t word = gather_sf_word(s);
   const int64_t c4 = K / 64;
   for (int j = 0; j < k; ++j) {
-    const int64_t f = t * k + j;
-    const int e = topk_ids[f];
-    const int64_t prow = (int64_t)pad_off[e] + flat_to_perm[f] - offsets[e];
+    const int64_t prow = __shfl_sync(0xFFFFFFFFu, my_prow, j);
     if (valid) *reinterpret_cast<uint2*>(a_codes + prow * (K / 2) + col0 / 2) = make_uint2(w0, w1);
     if (valid && (lane & 3) == 0)
       *reinterpret_cast<uint32_t*>(a_sf + sf_tiled_offset(prow, col0 / 16, c4)) = word;

@@ -507,6 +507,13 @@ def run_ours(args, cfg):
         "tokens_per_s": tokens_s,
         "pct_fp4_peak": tflops / world / fp4_peak,
         "pct_hbm_bw": nums["bytes"] / (ms * 1e-3) / 1e9 / hbm_peak,
+        # the layer against its own roofline: the larger of the two bounds over the time
+        "layer_roofline_frac": max(tflops / world / fp4_peak, nums["bytes"] / (ms * 1e-3) / 1e9 / hbm_peak),
+        # bytes of the intermediates between the kernels, reported apart from the
+        # algorithmic bytes (A in FP4 + scales, h in FP4 + scales, L2 output written and
+        # read back by the combine)
+        "pipeline_bytes": {"a_fp4": cfg.M * (K // 2 + K // 16), "h_fp4": cfg.M * (I // 2 + I // 16),
+                           "l2_out_bf16": 2 * cfg.M * K * 2},
         "layer_bytes": nums["bytes"], "layer_flops": nums["flops"],
         "stages_ms": stage_ms,
         "roofline": roof,

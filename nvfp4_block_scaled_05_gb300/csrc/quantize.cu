@@ -130,10 +130,11 @@ __global__ void __launch_bounds__(256) dispatch_quantize_kernel(
 // -> RoPE -> NVFP4 quant" in one pass).
 //
 // A row of nb = D/16 blocks is handled by a group of G lanes (G a power of two,
-// 4 <= G <= 32, the smallest with G * BPL >= nb); lane l of the group owns the
-// blocks l, l + G, ..., up to BPL of them, held in registers, so the row is
-// read once. Rows longer than 32 * BPL_MAX blocks take the second kernel
-// below, which streams the row twice. Per row: the sum of squares (per lane in
+// 4 <= G <= 32) whose lanes own up to BPL = 3 blocks each (lane l: blocks l,
+// l + G, ...), held in registers, so the row is read once; each group strides
+// over rows and loads its next row while it processes the current one. Rows
+// of more than 96 blocks take the second kernel below, which streams the row
+// twice. Per row: the sum of squares (per lane in
 // block order, then a butterfly over the group), y = x * (1/sqrt(mean + eps))
 // * gamma, the adjacent pairs of the rope blocks rotated with the tables at
 // the row's position, then each block quantized with the pre-computed global
@@ -222,47 +223,70 @@ __device__ __forceinline__ void norm_rope_store_sf(const NormRopeArgs& a, int64_
 }
 
 template <int G, int BPL>
-__global__ void __launch_bounds__(256) norm_rope_quantize_kernel(const NormRopeArgs a) {
+__global__ void __launch_bounds__(256, 2) norm_rope_quantize_kernel(const NormRopeArgs a) {
   const int lane = threadIdx.x & 31, gl = lane % G;
-  const int64_t r = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / G;
   const unsigned gmask = G == 32 ? 0xFFFFFFFFu : (((1u << G) - 1u) << (lane - gl));
-  if (r >= a.rows) return;   // whole groups leave together (rows are per group)
+  const int64_t ngroups = (int64_t)gridDim.x * blockDim.x / G;
   const int64_t nb = a.D / 16, rope0 = (a.D - a.R) / 16;
-  const __nv_bfloat16* xr = a.x + r * a.ldx;
-  const int32_t pos = a.R > 0 ? a.positions[r] : 0;
-  const bool bad = a.R > 0 && (pos < 0 || pos >= a.max_pos);
-  if (bad && gl == 0 && atomicCAS(&a.status[0], 0, NVFP4MOE_ERR_INVALID) == 0) a.status[1] = 10;
-  float v[BPL][16];
-  float ss = 0.0f;
-#pragma unroll
-  for (int i = 0; i < BPL; ++i) {
-    const int64_t b = gl + (int64_t)G * i;
-    if (b < nb) {
-      const uint4* p = reinterpret_cast<const uint4*>(xr + 16 * b);
-      bf16x8_to_f32(__ldg(p), v[i]);
-      bf16x8_to_f32(__ldg(p + 1), v[i] + 8);
-#pragma unroll
-      for (int e = 0; e < 16; ++e) ss = fmaf(v[i][e], v[i][e], ss);
-    }
-  }
-#pragma unroll
-  for (int o = G / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(gmask, ss, o);
-  const float inv = rsqrtf(ss / (float)a.D + a.eps);
   const float gs = *a.gs;
   // 4-byte scale words need 4 consecutive blocks in 4 consecutive lanes
   const bool words = (nb % 4) == 0 && G >= 4;
+  // Each group strides over rows; the BF16 blocks of its next row are loaded
+  // while the current row is processed.
+  auto load_row = [&](int64_t r, uint4 (&raw)[BPL][2]) {
+    const __nv_bfloat16* xr = a.x + r * a.ldx;
 #pragma unroll
-  for (int i = 0; i < BPL; ++i) {
-    const int64_t b = gl + (int64_t)G * i;
-    uint32_t sfb = 0;
-    if (b < nb) {
-      norm_rope_block(a, b, rope0, pos, bad, inv, v[i]);
-      sfb = norm_rope_store(a, r, b, gs, v[i]);
+    for (int i = 0; i < BPL; ++i) {
+      const int64_t b = gl + (int64_t)G * i;
+      if (b < nb) {
+        const uint4* p = reinterpret_cast<const uint4*>(xr + 16 * b);
+        raw[i][0] = __ldg(p);
+        raw[i][1] = __ldg(p + 1);
+      }
     }
-    const uint32_t b1 = __shfl_down_sync(gmask, sfb, 1, G);
-    const uint32_t b2 = __shfl_down_sync(gmask, sfb, 2, G);
-    const uint32_t b3 = __shfl_down_sync(gmask, sfb, 3, G);
-    if (b < nb) norm_rope_store_sf(a, r, b, sfb, sfb | (b1 << 8) | (b2 << 16) | (b3 << 24), words);
+  };
+  int64_t r = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / G;
+  uint4 cur[BPL][2], nxt[BPL][2];
+  if (r < a.rows) load_row(r, cur);
+  for (; r < a.rows; r += ngroups) {     // group-uniform: whole groups loop together
+    const int64_t rn = r + ngroups;
+    if (rn < a.rows) load_row(rn, nxt);
+    const int32_t pos = a.R > 0 ? a.positions[r] : 0;
+    const bool bad = a.R > 0 && (pos < 0 || pos >= a.max_pos);
+    if (bad && gl == 0 && atomicCAS(&a.status[0], 0, NVFP4MOE_ERR_INVALID) == 0) a.status[1] = 10;
+    float v[BPL][16];
+    float ss = 0.0f;
+#pragma unroll
+    for (int i = 0; i < BPL; ++i) {
+      const int64_t b = gl + (int64_t)G * i;
+      if (b < nb) {
+        bf16x8_to_f32(cur[i][0], v[i]);
+        bf16x8_to_f32(cur[i][1], v[i] + 8);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) ss = fmaf(v[i][e], v[i][e], ss);
+      }
+    }
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(gmask, ss, o);
+    const float inv = rsqrtf(ss / (float)a.D + a.eps);
+#pragma unroll
+    for (int i = 0; i < BPL; ++i) {
+      const int64_t b = gl + (int64_t)G * i;
+      uint32_t sfb = 0;
+      if (b < nb) {
+        norm_rope_block(a, b, rope0, pos, bad, inv, v[i]);
+        sfb = norm_rope_store(a, r, b, gs, v[i]);
+      }
+      const uint32_t b1 = __shfl_down_sync(gmask, sfb, 1, G);
+      const uint32_t b2 = __shfl_down_sync(gmask, sfb, 2, G);
+      const uint32_t b3 = __shfl_down_sync(gmask, sfb, 3, G);
+      if (b < nb) norm_rope_store_sf(a, r, b, sfb, sfb | (b1 << 8) | (b2 << 16) | (b3 << 24), words);
+    }
+#pragma unroll
+    for (int i = 0; i < BPL; ++i) {
+      cur[i][0] = nxt[i][0];
+      cur[i][1] = nxt[i][1];
+    }
   }
 }
 
@@ -303,8 +327,11 @@ __global__ void __launch_bounds__(256) norm_rope_quantize_long_kernel(const Norm
 
 template <int G, int BPL>
 void launch_norm_rope(const NormRopeArgs& a, cudaStream_t s) {
-  const int64_t threads = a.rows * G;
-  norm_rope_quantize_kernel<G, BPL><<<(unsigned)ceil_div(threads, 256), 256, 0, s>>>(a);
+  // enough groups to fill every SM (8 blocks of 256 threads each), no more than the rows
+  const int64_t groups_per_block = 256 / G;
+  const int64_t want = (int64_t)device_num_sms() * 8;
+  const int64_t need = ceil_div(a.rows, groups_per_block);
+  norm_rope_quantize_kernel<G, BPL><<<(unsigned)(need < want ? need : want), 256, 0, s>>>(a);
 }
 
 int launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ldx, const int32_t* row_src,
@@ -408,13 +435,14 @@ extern "C" int nvfp4_rmsnorm_rope_quantize(const void* x, int64_t rows, int64_t 
   NormRopeArgs a{static_cast<const __nv_bfloat16*>(x), rows, D, ldx, gamma, eps, rope_dims, positions,
                  cos_tab, sin_tab, max_pos, gs, codes, sf, sf_layout, y_out, status};
   cudaStream_t s = as_stream(stream);
+  // lane groups of G lanes with up to BPL blocks each: G * BPL covers the row
   const int64_t nb = D / 16;
   if (nb <= 4) launch_norm_rope<4, 1>(a, s);
-  else if (nb <= 8) launch_norm_rope<8, 1>(a, s);
-  else if (nb <= 16) launch_norm_rope<16, 1>(a, s);
-  else if (nb <= 32) launch_norm_rope<32, 1>(a, s);
-  else if (nb <= 64) launch_norm_rope<32, 2>(a, s);
-  else if (nb <= 128) launch_norm_rope<32, 4>(a, s);
+  else if (nb <= 8) launch_norm_rope<4, 2>(a, s);
+  else if (nb <= 12) launch_norm_rope<4, 3>(a, s);
+  else if (nb <= 24) launch_norm_rope<8, 3>(a, s);
+  else if (nb <= 48) launch_norm_rope<16, 3>(a, s);
+  else if (nb <= 96) launch_norm_rope<32, 3>(a, s);
   else norm_rope_quantize_long_kernel<<<(unsigned)ceil_div(rows, 8), 256, 0, s>>>(a);
   return launch_status();
 }

@@ -277,6 +277,14 @@ __device__ __forceinline__ void st_global_32B(void* p, uint32_t a0, uint32_t a1,
                : "memory");
 }
 
+// The same, marked as streaming (written once, read once much later: evicted first).
+__device__ __forceinline__ void st_global_32B_stream(void* p, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                                     uint32_t a4, uint32_t a5, uint32_t a6, uint32_t a7) {
+  asm volatile("st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a0), "r"(a1), "r"(a2),
+               "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
+               : "memory");
+}
+
 // Prefetch the box of a 2-D tiled TMA copy into L2 (no shared memory, no
 // completion: a hint that shortens the later load's latency).
 __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {

@@ -523,8 +523,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (p.c_32B) {
 #pragma unroll
           for (int j = 0; j < 8; ++j)
-            st_global_32B(out + 16 * j, packed[8 * j], packed[8 * j + 1], packed[8 * j + 2], packed[8 * j + 3],
-                          packed[8 * j + 4], packed[8 * j + 5], packed[8 * j + 6], packed[8 * j + 7]);
+            st_global_32B_stream(out + 16 * j, packed[8 * j], packed[8 * j + 1], packed[8 * j + 2],
+                                 packed[8 * j + 3], packed[8 * j + 4], packed[8 * j + 5], packed[8 * j + 6],
+                                 packed[8 * j + 7]);
         } else {
           uint4* dst = reinterpret_cast<uint4*>(out);
 #pragma unroll

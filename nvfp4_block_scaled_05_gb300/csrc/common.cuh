@@ -70,18 +70,16 @@ __device__ __forceinline__ uint32_t f32_to_e4m3_satfinite(float v) {
 }
 
 // Two E2M1 codes in one byte: `lo` in bits 0-3, `hi` in bits 4-7; round to
-// nearest even with saturation at 6. The sign bit of each code is taken from
-// the sign bit of its input, so a negative value that rounds to magnitude 0
-// is encoded as 0x8 whatever the conversion instruction does with zeros.
+// nearest even with saturation at 6. The conversion keeps the sign of its
+// input in every case, zeros included (checked on sm_103a for -0, negative
+// values that round to 0, negative subnormals: all give 0x8), so a negative
+// value that rounds to magnitude 0 is encoded as 0x8.
 __device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
   uint16_t r;
   asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u16.u8 %0, t;\n\t}"
       : "=h"(r)
       : "f"(hi), "f"(lo));
-  uint32_t b = r & 0xFFu;
-  b |= (__float_as_uint(lo) >> 31) << 3;
-  b |= (__float_as_uint(hi) >> 31) << 7;
-  return b;
+  return r & 0xFFu;
 }
 
 // RN(a / s) for an E4M3 block scale s > 0, given rcp = RN(1 / s): the product
@@ -283,6 +281,11 @@ __device__ __forceinline__ void st_global_32B_stream(void* p, uint32_t a0, uint3
   asm volatile("st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a0), "r"(a1), "r"(a2),
                "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
                : "memory");
+}
+
+// 8-byte global store marked as streaming (evict first).
+__device__ __forceinline__ void st_global_8B_stream(void* p, uint32_t a0, uint32_t a1) {
+  asm volatile("st.global.cs.v2.b32 [%0], {%1, %2};" ::"l"(p), "r"(a0), "r"(a1) : "memory");
 }
 
 // Prefetch the box of a 2-D tiled TMA copy into L2 (no shared memory, no

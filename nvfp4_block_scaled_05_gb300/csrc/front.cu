@@ -216,7 +216,7 @@ __global__ void __launch_bounds__(kFrontThreads) moe_front_kernel(const FrontPar
     for (int j = 0; j < k; ++j) {
       const int e = slot_e[tl * k + j];
       const int64_t prow = (int64_t)pad[e] + slot_pos[tl * k + j] - offs[e];
-      if (valid) *reinterpret_cast<uint2*>(p.a_codes + prow * (p.K / 2) + col0 / 2) = make_uint2(w0, w1);
+      if (valid) st_global_8B_stream(p.a_codes + prow * (p.K / 2) + col0 / 2, w0, w1);
       if (valid && (lane & 3) == 0)
         *reinterpret_cast<uint32_t*>(p.a_sf + sf_tiled_offset(prow, col0 / 16, c4)) = word;
     }

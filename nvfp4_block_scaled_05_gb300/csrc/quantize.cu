@@ -15,24 +15,41 @@ constexpr int kWarpsPerBlock = 8;
 constexpr int kChunk = 512;  // elements per warp
 
 // Largest |x| over the rows read, as the bit pattern of a non-negative f32
-// (atomicMax on the bits orders non-negative floats correctly).
+// (atomicMax on the bits orders non-negative floats correctly). Each thread
+// keeps four 16-byte loads in flight; kContig: no row gather and ldx == cols,
+// so the rows are one flat array.
+template <bool kContig>
 __global__ void __launch_bounds__(256) amax_rows_kernel(const __nv_bfloat16* __restrict__ x,
                                                         int64_t rows, int64_t cols, int64_t ldx,
                                                         const int32_t* __restrict__ row_src,
                                                         uint32_t* __restrict__ amax_bits) {
   const int64_t vec_per_row = cols / 8;
   const int64_t total = rows * vec_per_row;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   float m = 0.0f;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = i / vec_per_row, v = i - r * vec_per_row;
-    const int64_t src = row_src ? row_src[r] : r;
-    if (src < 0) continue;
-    const uint4 u = __ldg(reinterpret_cast<const uint4*>(x + src * ldx) + v);
-    float f[8];
-    bf16x8_to_f32(u, f);
+  for (int64_t i0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i0 < total; i0 += 4 * stride) {
+    uint4 u[4];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(f[j]));
+    for (int j = 0; j < 4; ++j) {
+      const int64_t i = i0 + j * stride;
+      u[j] = make_uint4(0u, 0u, 0u, 0u);
+      if (i < total) {
+        if (kContig) {
+          u[j] = __ldg(reinterpret_cast<const uint4*>(x) + i);
+        } else {
+          const int64_t r = i / vec_per_row, v = i - r * vec_per_row;
+          const int64_t src = row_src ? row_src[r] : r;
+          if (src >= 0) u[j] = __ldg(reinterpret_cast<const uint4*>(x + src * ldx) + v);
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float f[8];
+      bf16x8_to_f32(u[j], f);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) m = fmaxf(m, fabsf(f[c]));
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
@@ -120,7 +137,9 @@ __global__ void __launch_bounds__(256) dispatch_quantize_kernel(
   const int64_t c4 = K / 64;
   for (int j = 0; j < k; ++j) {
     const int64_t prow = __shfl_sync(0xFFFFFFFFu, my_prow, j);
-    if (valid) *reinterpret_cast<uint2*>(a_codes + prow * (K / 2) + col0 / 2) = make_uint2(w0, w1);
+    // codes stream past L2 (264 MB at 65536 rows); the scale words, four bytes
+    // of a 32-byte sector from each of eight rows, stay until their sector is whole
+    if (valid) st_global_8B_stream(a_codes + prow * (K / 2) + col0 / 2, w0, w1);
     if (valid && (lane & 3) == 0)
       *reinterpret_cast<uint32_t*>(a_sf + sf_tiled_offset(prow, col0 / 16, c4)) = word;
   }
@@ -131,9 +150,12 @@ __global__ void __launch_bounds__(256) dispatch_quantize_kernel(
 //
 // A row of nb = D/16 blocks is handled by a group of G lanes (G a power of two,
 // 4 <= G <= 32) whose lanes own up to BPL = 3 blocks each (lane l: blocks l,
-// l + G, ...), held in registers, so the row is read once; each group strides
-// over rows and loads its next row while it processes the current one. Rows
-// of more than 96 blocks take the second kernel below, which streams the row
+// l + G, ...), held in registers as BF16, so the row is read once; each group
+// strides over rows. Measured on the 192-wide q-head rows: keeping only the
+// BF16 words live (each block is widened to f32 twice, for the sum of squares
+// and for the rest) lets 3 blocks of 256 threads share an SM, 25% faster than
+// 2 blocks that also held the f32 values and the next row's loads. Rows of
+// more than 96 blocks take the second kernel below, which streams the row
 // twice. Per row: the sum of squares (per lane in
 // block order, then a butterfly over the group), y = x * (1/sqrt(mean + eps))
 // * gamma, the adjacent pairs of the rope blocks rotated with the tables at
@@ -223,7 +245,7 @@ __device__ __forceinline__ void norm_rope_store_sf(const NormRopeArgs& a, int64_
 }
 
 template <int G, int BPL>
-__global__ void __launch_bounds__(256, 2) norm_rope_quantize_kernel(const NormRopeArgs a) {
+__global__ void __launch_bounds__(256, 3) norm_rope_quantize_kernel(const NormRopeArgs a) {
   const int lane = threadIdx.x & 31, gl = lane % G;
   const unsigned gmask = G == 32 ? 0xFFFFFFFFu : (((1u << G) - 1u) << (lane - gl));
   const int64_t ngroups = (int64_t)gridDim.x * blockDim.x / G;
@@ -231,8 +253,6 @@ __global__ void __launch_bounds__(256, 2) norm_rope_quantize_kernel(const NormRo
   const float gs = *a.gs;
   // 4-byte scale words need 4 consecutive blocks in 4 consecutive lanes
   const bool words = (nb % 4) == 0 && G >= 4;
-  // Each group strides over rows; the BF16 blocks of its next row are loaded
-  // while the current row is processed.
   auto load_row = [&](int64_t r, uint4 (&raw)[BPL][2]) {
     const __nv_bfloat16* xr = a.x + r * a.ldx;
 #pragma unroll
@@ -246,24 +266,22 @@ __global__ void __launch_bounds__(256, 2) norm_rope_quantize_kernel(const NormRo
     }
   };
   int64_t r = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / G;
-  uint4 cur[BPL][2], nxt[BPL][2];
-  if (r < a.rows) load_row(r, cur);
+  uint4 cur[BPL][2];
   for (; r < a.rows; r += ngroups) {     // group-uniform: whole groups loop together
-    const int64_t rn = r + ngroups;
-    if (rn < a.rows) load_row(rn, nxt);
+    load_row(r, cur);
     const int32_t pos = a.R > 0 ? a.positions[r] : 0;
     const bool bad = a.R > 0 && (pos < 0 || pos >= a.max_pos);
     if (bad && gl == 0 && atomicCAS(&a.status[0], 0, NVFP4MOE_ERR_INVALID) == 0) a.status[1] = 10;
-    float v[BPL][16];
     float ss = 0.0f;
 #pragma unroll
     for (int i = 0; i < BPL; ++i) {
       const int64_t b = gl + (int64_t)G * i;
       if (b < nb) {
-        bf16x8_to_f32(cur[i][0], v[i]);
-        bf16x8_to_f32(cur[i][1], v[i] + 8);
+        float v[16];
+        bf16x8_to_f32(cur[i][0], v);
+        bf16x8_to_f32(cur[i][1], v + 8);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) ss = fmaf(v[i][e], v[i][e], ss);
+        for (int e = 0; e < 16; ++e) ss = fmaf(v[e], v[e], ss);
       }
     }
 #pragma unroll
@@ -274,18 +292,16 @@ __global__ void __launch_bounds__(256, 2) norm_rope_quantize_kernel(const NormRo
       const int64_t b = gl + (int64_t)G * i;
       uint32_t sfb = 0;
       if (b < nb) {
-        norm_rope_block(a, b, rope0, pos, bad, inv, v[i]);
-        sfb = norm_rope_store(a, r, b, gs, v[i]);
+        float v[16];
+        bf16x8_to_f32(cur[i][0], v);
+        bf16x8_to_f32(cur[i][1], v + 8);
+        norm_rope_block(a, b, rope0, pos, bad, inv, v);
+        sfb = norm_rope_store(a, r, b, gs, v);
       }
       const uint32_t b1 = __shfl_down_sync(gmask, sfb, 1, G);
       const uint32_t b2 = __shfl_down_sync(gmask, sfb, 2, G);
       const uint32_t b3 = __shfl_down_sync(gmask, sfb, 3, G);
       if (b < nb) norm_rope_store_sf(a, r, b, sfb, sfb | (b1 << 8) | (b2 << 16) | (b3 << 24), words);
-    }
-#pragma unroll
-    for (int i = 0; i < BPL; ++i) {
-      cur[i][0] = nxt[i][0];
-      cur[i][1] = nxt[i][1];
     }
   }
 }
@@ -327,9 +343,14 @@ __global__ void __launch_bounds__(256) norm_rope_quantize_long_kernel(const Norm
 
 template <int G, int BPL>
 void launch_norm_rope(const NormRopeArgs& a, cudaStream_t s) {
-  // enough groups to fill every SM (8 blocks of 256 threads each), no more than the rows
+  // as many blocks as are resident at once (each strides over the rows), no
+  // more than the rows need
+  static int per_sm = 0;
+  if (per_sm == 0 &&
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, norm_rope_quantize_kernel<G, BPL>, 256, 0) != cudaSuccess)
+    per_sm = 0;
   const int64_t groups_per_block = 256 / G;
-  const int64_t want = (int64_t)device_num_sms() * 8;
+  const int64_t want = (int64_t)device_num_sms() * (per_sm > 0 ? per_sm : 2);
   const int64_t need = ceil_div(a.rows, groups_per_block);
   norm_rope_quantize_kernel<G, BPL><<<(unsigned)(need < want ? need : want), 256, 0, s>>>(a);
 }
@@ -339,10 +360,16 @@ int launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ldx, const in
   if (cudaMemsetAsync(amax_bits, 0, sizeof(uint32_t), s) != cudaSuccess) return NVFP4MOE_ERR_LAUNCH;
   const int64_t total = rows * (cols / 8);
   if (total > 0) {
-    int64_t blocks = (total + 255) / 256;
-    int64_t cap = 4096;
-    amax_rows_kernel<<<(unsigned)(blocks < cap ? blocks : cap), 256, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(x), rows, cols, ldx, row_src, amax_bits);
+    // 8 blocks of 256 threads per SM, fewer when there is not enough work for
+    // four loads per thread
+    const int64_t blocks = ceil_div(total, 256 * 4);
+    const int64_t cap = (int64_t)device_num_sms() * 8;
+    const unsigned grid = (unsigned)(blocks < cap || cap <= 0 ? blocks : cap);
+    const auto* xb = static_cast<const __nv_bfloat16*>(x);
+    if (!row_src && ldx == cols)
+      amax_rows_kernel<true><<<grid, 256, 0, s>>>(xb, rows, cols, ldx, row_src, amax_bits);
+    else
+      amax_rows_kernel<false><<<grid, 256, 0, s>>>(xb, rows, cols, ldx, row_src, amax_bits);
   }
   return launch_status();
 }

@@ -58,6 +58,8 @@ def test_quantize_signed_zero_and_ties():
     x = torch.from_numpy(np.tile(vals, (4, 1))).to(torch.bfloat16)
     codes, _ = _quant_check(x, gs_given=1.0)
     assert codes[0, 8] & 0xF0 == 0x80            # -0.1 -> code 0x8
+    assert codes[0, 9] & 0x0F == 0x08            # -0.0 in a nonzero block -> code 0x8
+    assert codes[0, 10] & 0x0F == 0x08           # -0.01 -> code 0x8
 
 
 def test_quantize_linear_workload_edge_blocks():

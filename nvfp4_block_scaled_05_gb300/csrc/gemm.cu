@@ -533,15 +533,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             dst[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
         }
       } else {
-        uint32_t u[2][64];
-        tc_ld64_wait(taddr, u[0]);
-        tc_ld64_wait(taddr + 64, u[1]);
-        const float* v = reinterpret_cast<const float*>(u);
+        // columns 32*b + [0,8) gate / [8,16) up of h features 16b..16b+7,
+        // columns 32*b + [16,24) gate / [24,32) up of h features 16b+8..16b+15.
+        // The first 64 columns become 32 h values before the second 64 are
+        // loaded, so at most 96 values are live (the 128-register cap would
+        // otherwise spill); the accumulator is released after the second load.
+        float hv[32];
+        {
+          uint32_t u0[64];
+          tc_ld64_wait(taddr, u0);
+          const float* v0 = reinterpret_cast<const float*>(u0);
+#pragma unroll
+          for (int b = 0; b < 2; ++b)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              hv[16 * b + i] = silu(v0[32 * b + i] * alpha) * (v0[32 * b + 8 + i] * alpha);
+              hv[16 * b + 8 + i] = silu(v0[32 * b + 16 + i] * alpha) * (v0[32 * b + 24 + i] * alpha);
+            }
+        }
+        uint32_t u1[64];
+        tc_ld64_wait(taddr + 64, u1);
+        const float* v1 = reinterpret_cast<const float*>(u1);
         tc_fence_before();
         mbar_arrive(bar_acce);
         if (!active) continue;
-        // columns 32*b + [0,8) gate / [8,16) up of h features 16b..16b+7,
-        // columns 32*b + [16,24) gate / [24,32) up of h features 16b+8..16b+15
         const float gs_h = *p.gs_h;
         const int64_t hrow = (int64_t)pad_off[e] + mb * BM + row;
         const int64_t hfeat = (int64_t)nb * (BN / 2) + half * 64;   // first h feature of this thread
@@ -550,10 +565,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
           float h[16];
+          if (b < 2) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            h[i] = silu(v[32 * b + i] * alpha) * (v[32 * b + 8 + i] * alpha);
-            h[8 + i] = silu(v[32 * b + 16 + i] * alpha) * (v[32 * b + 24 + i] * alpha);
+            for (int i = 0; i < 16; ++i) h[i] = hv[16 * b + i];
+          } else {
+            const float* v = v1 + 32 * (b - 2);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              h[i] = silu(v[i] * alpha) * (v[8 + i] * alpha);
+              h[8 + i] = silu(v[16 + i] * alpha) * (v[24 + i] * alpha);
+            }
           }
           const uint32_t sf = quantize_block16(h, gs_h, words[2 * b], words[2 * b + 1]);
           sfw |= sf << (8 * b);

@@ -111,7 +111,12 @@ __device__ __forceinline__ uint32_t quantize_block16(const float (&v)[16], float
     w1 = 0u;
     return 0u;
   }
-  const uint32_t sf = f32_to_e4m3_satfinite(__fdiv_rn(p, 6.0f));
+  // p / 6 by the same FMA-corrected product (6 is an E4M3 value, so the
+  // exhaustive check covers it; p >= 6 * 2^-9 keeps everything normal). From
+  // p = 2688 on the scale saturates at 448 whatever the rounding; a plain
+  // division there keeps even an infinite p exact.
+  const float p6 = p < 2688.0f ? div_by_scale(p, 6.0f, 0x1.555556p-3f) : __fdiv_rn(p, 6.0f);
+  const uint32_t sf = f32_to_e4m3_satfinite(p6);
   const float s = e4m3_to_f32(sf);
   const float rcp = __frcp_rn(s);
   uint32_t b[8];

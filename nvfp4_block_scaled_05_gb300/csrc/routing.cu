@@ -59,11 +59,18 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ c
   __shared__ int32_t warp_sums[32];
   const int e = threadIdx.x;
   int total = 0;
+  // the chunks' counts of expert e become exclusive prefixes; 16 loads are in
+  // flight at a time (one at a time, the loop was a chain of L2 round trips)
   if (e < E) {
-    for (int c = 0; c < nchunk; ++c) {
-      const int v = counts[(int64_t)c * E + e];
-      counts[(int64_t)c * E + e] = total;
-      total += v;
+    for (int c0 = 0; c0 < nchunk; c0 += 16) {
+      int v[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = c0 + j < nchunk ? counts[(int64_t)(c0 + j) * E + e] : 0;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        if (c0 + j < nchunk) counts[(int64_t)(c0 + j) * E + e] = total;
+        total += v[j];
+      }
     }
   }
   // block-wide exclusive scan of the per-expert totals
@@ -90,7 +97,14 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ c
   const int excl = warp_sums[wid] + incl - total;
   if (e < E) {
     offsets[e] = excl;
-    for (int c = 0; c < nchunk; ++c) counts[(int64_t)c * E + e] += excl;
+    for (int c0 = 0; c0 < nchunk; c0 += 16) {
+      int v[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = c0 + j < nchunk ? counts[(int64_t)(c0 + j) * E + e] : 0;
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (c0 + j < nchunk) counts[(int64_t)(c0 + j) * E + e] = v[j] + excl;
+    }
   }
   if (e == 0) offsets[E] = (int32_t)n;
 }

@@ -293,20 +293,6 @@ __device__ __forceinline__ void st_global_8B_stream(void* p, uint32_t a0, uint32
   asm volatile("st.global.cs.v2.b32 [%0], {%1, %2};" ::"l"(p), "r"(a0), "r"(a1) : "memory");
 }
 
-// Prefetch the box of a 2-D tiled TMA copy into L2 (no shared memory, no
-// completion: a hint that shortens the later load's latency).
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y)
-               : "memory");
-}
-
-// Prefetch `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2.
-__device__ __forceinline__ void bulk_prefetch(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 // 16-byte asynchronous copy global -> shared through the load path (L2 only),
 // and an arrive on an mbarrier once all of this thread's earlier such copies
 // have landed (the barrier's count includes this arrival).
@@ -373,13 +359,6 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
                : "memory");
 }
 
-// Copy 32 rows x 16 bytes of shared memory into 4 TMEM columns of 32 lanes,
-// replicated into all four lane quadrants.
-__device__ __forceinline__ void tc_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
-               : "memory");
-}
-
 // D (TMEM, f32) (+)= A * B^T with both operands NVFP4 (E2M1 + UE4M3 scale per
 // 16 elements along K), M=128, K=64 per instruction.
 __device__ __forceinline__ void tc_mma_nvf4(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
@@ -438,16 +417,6 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
   d |= static_cast<uint64_t>(1024 >> 4) << 32;            // stride byte offset
   d |= static_cast<uint64_t>(1) << 46;                    // descriptor version
   d |= static_cast<uint64_t>(2) << 61;                    // 128-byte swizzle
-  return d;
-}
-
-// Descriptor of 32 rows x 16 contiguous bytes (no swizzle), the source of a
-// tcgen05.cp 32x128b copy of one 512-byte scale atom.
-__device__ __forceinline__ uint64_t sdesc_sf_atom(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>(128 >> 4) << 32;  // 8-row groups 128 bytes apart
-  d |= static_cast<uint64_t>(1) << 46;
   return d;
 }
 

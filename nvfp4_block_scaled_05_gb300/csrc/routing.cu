@@ -116,12 +116,21 @@ __global__ void __launch_bounds__(32) perm_scatter_kernel(const int32_t* __restr
   extern __shared__ int32_t next[];
   const int lane = threadIdx.x;
   for (int e = lane; e < E; e += 32) next[e] = base[blockIdx.x * (int64_t)E + e];
-  __syncwarp();
   const int64_t f0 = blockIdx.x * (int64_t)kPermChunk;
-  for (int i = 0; i < kPermChunk; i += 32) {
-    const int64_t f = f0 + i + lane;
+  // the chunk's experts are all loaded up front: the ordered walk below is
+  // then a chain of shared-memory and warp operations, not of global loads
+  int ev[kPermChunk / 32];
+#pragma unroll
+  for (int i = 0; i < kPermChunk / 32; ++i) {
+    const int64_t f = f0 + 32 * i + lane;
+    ev[i] = f < n ? ids[f] : -1 - lane;  // invalid lanes never match a real expert
+  }
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < kPermChunk / 32; ++i) {
+    const int64_t f = f0 + 32 * i + lane;
     const bool valid = f < n;
-    const int e = valid ? ids[f] : -1 - lane;  // invalid lanes never match a real expert
+    const int e = ev[i];
     const uint32_t peers = __match_any_sync(0xFFFFFFFFu, e);
     const int rank = __popc(peers & ((1u << lane) - 1u));
     const int start = valid ? next[e] : 0;

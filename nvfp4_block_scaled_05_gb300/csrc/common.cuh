@@ -52,8 +52,13 @@ int moe_front(const void* x, int64_t ldx, const float* logits, int64_t T, int64_
 
 // Byte offset of the scale of (row r, 16-element block b) in the tiled layout
 // documented in nvfp4moe.h.
+// It is the sum of a row part and a block part (c4 = column groups of 64).
+__host__ __device__ inline int64_t sf_tiled_row_part(int64_t r, int64_t c4) {
+  return (r >> 7) * c4 * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4;
+}
+__host__ __device__ inline int64_t sf_tiled_block_part(int64_t b) { return (b >> 2) * 512 + (b & 3); }
 __host__ __device__ inline int64_t sf_tiled_offset(int64_t r, int64_t b, int64_t c4) {
-  return ((r >> 7) * c4 + (b >> 2)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + (b & 3);
+  return sf_tiled_row_part(r, c4) + sf_tiled_block_part(b);
 }
 
 // ------------------------------------------------------------------ NVFP4 encode

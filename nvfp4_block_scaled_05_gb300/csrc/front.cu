@@ -210,15 +210,24 @@ __global__ void __launch_bounds__(kFrontThreads) moe_front_kernel(const FrontPar
     const int tl = item / nchunk;
     const int64_t col0 = (int64_t)(item - tl * nchunk) * 512 + lane * 16;
     const bool valid = col0 < p.K;
+    // lane j < k: the padded row of the token's slot j, as the row parts of
+    // its code and scale addresses
+    unsigned long long my_codes = 0, my_sf = 0;
+    if (lane < k) {
+      const int e = slot_e[tl * k + lane];
+      const int64_t prow = (int64_t)pad[e] + slot_pos[tl * k + lane] - offs[e];
+      my_codes = reinterpret_cast<unsigned long long>(p.a_codes + prow * (p.K / 2));
+      my_sf = reinterpret_cast<unsigned long long>(p.a_sf + sf_tiled_row_part(prow, c4));
+    }
     uint32_t w0 = 0, w1 = 0, s = 0;
     if (valid) s = quantize_lane16(p.x + (t0 + tl) * p.ldx, col0, gs, w0, w1);
     const uint32_t word = gather_sf_word(s);
+    const int64_t code_col = col0 / 2, sf_col = sf_tiled_block_part(col0 / 16);
     for (int j = 0; j < k; ++j) {
-      const int e = slot_e[tl * k + j];
-      const int64_t prow = (int64_t)pad[e] + slot_pos[tl * k + j] - offs[e];
-      if (valid) st_global_8B_stream(p.a_codes + prow * (p.K / 2) + col0 / 2, w0, w1);
-      if (valid && (lane & 3) == 0)
-        *reinterpret_cast<uint32_t*>(p.a_sf + sf_tiled_offset(prow, col0 / 16, c4)) = word;
+      uint8_t* dc = reinterpret_cast<uint8_t*>(__shfl_sync(0xFFFFFFFFu, my_codes, j));
+      uint8_t* ds = reinterpret_cast<uint8_t*>(__shfl_sync(0xFFFFFFFFu, my_sf, j));
+      if (valid) st_global_8B_stream(dc + code_col, w0, w1);
+      if (valid && (lane & 3) == 0) *reinterpret_cast<uint32_t*>(ds + sf_col) = word;
     }
   }
 }

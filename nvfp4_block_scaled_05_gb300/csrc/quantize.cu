@@ -124,24 +124,29 @@ __global__ void __launch_bounds__(256) dispatch_quantize_kernel(
   if (t >= T) return;
   const int64_t col0 = (gw - t * nchunk) * kChunk + lane * 16;
   const bool valid = col0 < K;
-  // lane j < k finds the padded row of slot j while the row is being quantized
-  int my_prow = 0;
+  // lane j < k finds the padded row of slot j while the row is being quantized,
+  // and the row parts of its code and scale addresses (the warp's lanes then
+  // only add their column parts)
+  const int64_t c4 = K / 64;
+  unsigned long long my_codes = 0, my_sf = 0;
   if (lane < k) {
     const int64_t f = t * k + lane;
     const int e = topk_ids[f];
-    my_prow = pad_off[e] + flat_to_perm[f] - offsets[e];
+    const int64_t prow = pad_off[e] + flat_to_perm[f] - offsets[e];
+    my_codes = reinterpret_cast<unsigned long long>(a_codes + prow * (K / 2));
+    my_sf = reinterpret_cast<unsigned long long>(a_sf + sf_tiled_row_part(prow, c4));
   }
   uint32_t w0 = 0, w1 = 0, s = 0;
   if (valid) s = quantize_lane16(x + t * ldx, col0, gs, w0, w1);
   const uint32_t word = gather_sf_word(s);
-  const int64_t c4 = K / 64;
+  const int64_t code_col = col0 / 2, sf_col = sf_tiled_block_part(col0 / 16);
   for (int j = 0; j < k; ++j) {
-    const int64_t prow = __shfl_sync(0xFFFFFFFFu, my_prow, j);
+    uint8_t* dc = reinterpret_cast<uint8_t*>(__shfl_sync(0xFFFFFFFFu, my_codes, j));
+    uint8_t* ds = reinterpret_cast<uint8_t*>(__shfl_sync(0xFFFFFFFFu, my_sf, j));
     // codes stream past L2 (264 MB at 65536 rows); the scale words, four bytes
     // of a 32-byte sector from each of eight rows, stay until their sector is whole
-    if (valid) st_global_8B_stream(a_codes + prow * (K / 2) + col0 / 2, w0, w1);
-    if (valid && (lane & 3) == 0)
-      *reinterpret_cast<uint32_t*>(a_sf + sf_tiled_offset(prow, col0 / 16, c4)) = word;
+    if (valid) st_global_8B_stream(dc + code_col, w0, w1);
+    if (valid && (lane & 3) == 0) *reinterpret_cast<uint32_t*>(ds + sf_col) = word;
   }
 }
 

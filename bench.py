@@ -258,7 +258,7 @@ def full_size_parity(cfg, seed, n_experts, x, logits, dev, f2p, out, topk_w):
     L2 output rows and routing weights left in the workspace by the last timed
     forward, against the oracle's fp64 share on the same inputs (x and logits
     copied back, the sampled experts' weights drawn again on the device: the
-    same values as the run's), with the benchmark spec's tolerance."""
+    same values as the run's), with the layer tolerance (2e-2 * max(1, |y|))."""
     import numpy as np
     import oracle as O
     from nvfp4_block_scaled_05_gb300 import workloads as W
@@ -291,7 +291,7 @@ def full_size_parity(cfg, seed, n_experts, x, logits, dev, f2p, out, topk_w):
     rg, rw = np.array(rows_got), np.array(rows_want)
     rcos = float((rg * rw).sum() / np.sqrt((rg * rg).sum() * (rw * rw).sum()))
     parity = {"tokens": len(tix), "routed_rows": len(rows_got), "experts": experts,
-              "max_err_north_star": float(err.max()), "tolerance": 2e-2, "within": bool(err.max() <= 2e-2),
+              "max_err_over_tol": float(err.max()), "tolerance": 2e-2, "within": bool(err.max() <= 2e-2),
               "cosine": cos, "l2_rows_cosine": rcos,
               "compared": "the sampled experts' share of y for every token routed to them, formed from the "
                           "benchmarked run's L2 output rows and routing weights, against the fp64 oracle on "
@@ -304,17 +304,64 @@ def full_size_parity(cfg, seed, n_experts, x, logits, dev, f2p, out, topk_w):
     return parity, cpu
 
 
+_QW_CACHE = {}
+
+
+def oracle_step_sample(cfg, seed, step, max_rows, n_experts=4):
+    """One step of the reference arm: the tokens routed to one of the first
+    n_experts active experts (cycled by step), at most max_rows of them (None:
+    all). The experts' quantized weights are drawn once and kept, so a step
+    costs only the oracle's arithmetic."""
+    import numpy as np
+    import oracle as O
+    from nvfp4_block_scaled_05_gb300 import workloads as W
+    key = (cfg.name, seed)
+    if key not in _HOST_INPUTS:
+        inp = W.moe_inputs(cfg, seed=seed, device="cpu", weights=False)
+        lg = inp["logits"].numpy()
+        _HOST_INPUTS[key] = (W.bf16_bits(inp["x"]), lg, O.route_topk(lg, cfg.k)[0])
+    x, logits, ids = _HOST_INPUTS[key]
+    counts = np.bincount(ids.ravel(), minlength=cfg.E)
+    active = [e for e in range(cfg.E) if counts[e] > 0]
+    e = active[step % min(n_experts, len(active))]
+    if (key, e) not in _QW_CACHE:
+        c1, s1, g1 = O.quantize_expert(W.bf16_bits(W.expert_weight(cfg, seed, 1, e)))
+        c2, s2, g2 = O.quantize_expert(W.bf16_bits(W.expert_weight(cfg, seed, 2, e)))
+        _QW_CACHE[(key, e)] = (c1, s1, g1, c2, s2, g2)
+    tokens = sorted(set(int(t) for t in np.nonzero((ids == e).any(axis=1))[0]))
+    if max_rows is not None:
+        tokens = tokens[:max_rows]
+    return dict(x=x, logits=logits, experts=[e], qw={e: _QW_CACHE[(key, e)]}, tokens=tokens,
+                rows=len(tokens))
+
+
 def run_reference(args, cfg):
+    """The CPU oracle, timed on the host cores, on a bounded sample of the
+    workload: every step runs the routed rows of one expert (cycling over four
+    experts whose weights are prepared once), with the rows per step chosen
+    from two calibration calls so that all warm-up and timed steps together
+    take about two and a half minutes (longer only when the per-call cost
+    alone exceeds that: one row per step then)."""
     world, rank, _ = dist_env()
     if rank != 0:
         return
     import oracle as O
-    n_exp = 1
-    samples = [oracle_sample(cfg, args.seed, n_exp, step=i) for i in range(args.warmup + args.steps)]
-    for s in samples[:args.warmup]:
-        time_oracle(cfg, s)
+    # calibration: a one-row call (the per-call cost: routing, permutation and
+    # global scale over all tokens, the expert's weights dequantized) and a
+    # whole-expert call (the cost per row)
+    one = oracle_step_sample(cfg, args.seed, 0, 1)
+    fixed, _ = time_oracle(cfg, one)
+    calib = oracle_step_sample(cfg, args.seed, 0, None)
+    dt0, _ = time_oracle(cfg, calib)
+    per_row = max(dt0 - fixed, 1e-6) / max(1, calib["rows"] - 1)
+    n_total = max(1, args.warmup + args.steps)
+    budget = 150.0 / n_total - fixed      # seconds of row work per step
+    max_rows = max(1, min(calib["rows"], int(budget / per_row) if budget > 0 else 1))
+    for i in range(args.warmup):
+        time_oracle(cfg, oracle_step_sample(cfg, args.seed, i, max_rows))
     total_t, total_f, rows = 0.0, 0.0, 0
-    for s in samples[args.warmup:]:
+    for i in range(args.steps):
+        s = oracle_step_sample(cfg, args.seed, args.warmup + i, max_rows)
         dt, fl = time_oracle(cfg, s)
         total_t += dt
         total_f += fl
@@ -325,11 +372,12 @@ def run_reference(args, cfg):
             "ms_per_step": total_t / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
             "config": {"workload": cfg.name, "T": cfg.T, "K": cfg.K, "I": cfg.I, "E": cfg.E, "k": cfg.k,
-                       "seed": args.seed, "step": "all routed rows of one expert per step"},
+                       "seed": args.seed,
+                       "step": "up to %d routed rows of one expert (of 4, cycled) per step" % max_rows},
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": O.get_threads(),
                              "kind": "oracle",
-                             "sample": "%d steps x all routed rows of one expert (%d rows in total)"
-                                       % (args.steps, rows)},
+                             "sample": "%d steps x up to %d routed rows of one expert (%d rows in total)"
+                                       % (args.steps, max_rows, rows)},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 

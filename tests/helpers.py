@@ -48,7 +48,7 @@ def to_np(t):
     return t.cpu().numpy()
 
 
-def assert_close_north_star(got, ref, what=""):
+def assert_close_tol(got, ref, what=""):
     """|gpu - oracle| <= 2e-2 * max(1, |oracle|) per element."""
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)

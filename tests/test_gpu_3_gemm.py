@@ -4,7 +4,7 @@ Inputs are built in the oracle's formats and laid out on the device with the
 documented layouts (grouped-padded rows, tiled scales), so both sides see the
 same bytes. Structured inputs (constant codes and scales) come first, so that a
 failure says which part of the operand layout is wrong; on failure the raw GPU
-output is saved under gpurun_out/ when that folder exists.
+output is saved to the folder named by NVFP4MOE_DUMP_DIR, when that is set.
 """
 import os
 
@@ -13,8 +13,7 @@ import pytest
 import torch
 
 import oracle as O
-from conftest import ROOT
-from helpers import (assert_close_north_star, cosine, padded_rows_of_compact, padded_starts,
+from helpers import (assert_close_tol, cosine, padded_rows_of_compact, padded_starts,
                      sf_tiled_index)
 from nvfp4_block_scaled_05_gb300 import binding as B
 
@@ -23,8 +22,8 @@ DEV = "cuda"
 
 
 def _dump(name, **arrays):
-    d = os.path.join(ROOT, "gpurun_out")
-    if os.path.isdir(d):
+    d = os.environ.get("NVFP4MOE_DUMP_DIR")
+    if d and os.path.isdir(d):
         np.savez(os.path.join(d, "fail_%s.npz" % name), **arrays)
 
 
@@ -94,14 +93,14 @@ def _run_grouped(rng, counts, N, K, mode_a="random", mode_b="random", name="g", 
 def test_single_tile_structured(mode):
     rng = np.random.default_rng(1)
     got, ref = _run_grouped(rng, [128], 128, 256, mode, mode, name="single_" + mode)
-    assert_close_north_star(got, ref, mode)
+    assert_close_tol(got, ref, mode)
     assert cosine(got, ref) > 0.9999
 
 
 def test_grouped_uneven_groups_and_empty_experts():
     rng = np.random.default_rng(2)
     got, ref = _run_grouped(rng, [5, 0, 130, 1, 0, 300, 17, 128], 256, 512, name="uneven")
-    assert_close_north_star(got, ref, "uneven")
+    assert_close_tol(got, ref, "uneven")
     assert cosine(got, ref) > 0.9999
     rel = np.abs(got - ref) / (np.abs(ref).max())
     assert rel.max() < 1e-2
@@ -111,7 +110,7 @@ def test_grouped_uneven_groups_and_empty_experts():
 def test_k_tails(K):
     rng = np.random.default_rng(K)
     got, ref = _run_grouped(rng, [40, 200], 128, K, name="k%d" % K)
-    assert_close_north_star(got, ref, "K=%d" % K)
+    assert_close_tol(got, ref, "K=%d" % K)
     assert cosine(got, ref) > 0.9999
 
 
@@ -121,7 +120,7 @@ def test_strided_output_matches_sector_path():
     got_w, ref = _run_grouped(np.random.default_rng(11), [70, 0, 200], 256, 512, name="wide", wide=True)
     got_p, _ = _run_grouped(np.random.default_rng(11), [70, 0, 200], 256, 512, name="packed")
     assert np.array_equal(got_w, got_p)
-    assert_close_north_star(got_w, ref, "wide")
+    assert_close_tol(got_w, ref, "wide")
 
 
 def test_linear_workload_sampled_rows():
@@ -147,7 +146,7 @@ def test_linear_workload_sampled_rows():
     got = c[torch.from_numpy(rows).to(DEV)].float().cpu().numpy()
     if not np.all(np.abs(got - ref) <= 2e-2 * np.maximum(1.0, np.abs(ref))):
         _dump("linear", got=got, ref=ref, rows=rows)
-    assert_close_north_star(got, ref, "linear")
+    assert_close_tol(got, ref, "linear")
     assert cosine(got, ref) > 0.9999
 
 

@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import oracle as O
-from helpers import (assert_close_north_star, cosine, padded_rows_of_compact, sf_tiled_index)
+from helpers import (assert_close_tol, cosine, padded_rows_of_compact, sf_tiled_index)
 from nvfp4_block_scaled_05_gb300 import binding as B
 from nvfp4_block_scaled_05_gb300 import workloads as W
 
@@ -64,7 +64,7 @@ def _run(cfg, seed, sample):
             assert np.array_equal(a_codes[p].cpu().numpy(), ref["x_codes"][ti])
             assert np.array_equal(a_sf[sf_idx[p]], ref["x_sf"][ti])
     got = y[torch.from_numpy(np.asarray(ref["tokens"])).to(DEV)].float().cpu().numpy()
-    assert_close_north_star(got, ref["y"], cfg.name)
+    assert_close_tol(got, ref["y"], cfg.name)
     c = cosine(got, ref["y"])
     assert c >= 0.9995, c
     return got, ref, y, inp, wts, gs_h
@@ -118,7 +118,7 @@ def test_moe_edge_shapes():
         xb, w1b, w2b = W.bf16_bits(x), W.bf16_bits(w1), W.bf16_bits(w2)
         ref = O.moe_forward(xb, logits.numpy(), lambda e: w1b[e], lambda e: w2b[e], k, np.float32(cfg.gs_h))
         got = y.float().cpu().numpy()
-        assert_close_north_star(got, ref["y"], "edge %s" % ((T, E, k, mode),))
+        assert_close_tol(got, ref["y"], "edge %s" % ((T, E, k, mode),))
         assert cosine(got, ref["y"]) >= 0.9995
 
 

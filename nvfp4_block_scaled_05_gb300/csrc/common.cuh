@@ -74,17 +74,23 @@ __device__ __forceinline__ uint32_t f32_to_e4m3_satfinite(float v) {
   return static_cast<uint32_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
 }
 
-// Two E2M1 codes in one byte: `lo` in bits 0-3, `hi` in bits 4-7; round to
-// nearest even with saturation at 6. The conversion keeps the sign of its
-// input in every case, zeros included (checked on sm_103a for -0, negative
-// values that round to 0, negative subnormals: all give 0x8), so a negative
-// value that rounds to magnitude 0 is encoded as 0x8.
-__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
-  uint16_t r;
-  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u16.u8 %0, t;\n\t}"
-      : "=h"(r)
-      : "f"(hi), "f"(lo));
-  return r & 0xFFu;
+// Eight E2M1 codes in one word: q[2j] in the low nibble and q[2j+1] in the
+// high nibble of byte j; round to nearest even with saturation at 6. The
+// conversion keeps the sign of its input in every case, zeros included
+// (checked on sm_103a for -0, negative values that round to 0, negative
+// subnormals: all give 0x8), so a negative value that rounds to magnitude 0
+// is encoded as 0x8.
+__device__ __forceinline__ uint32_t e2m1x8(const float (&q)[8]) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(r)
+      : "f"(q[0]), "f"(q[1]), "f"(q[2]), "f"(q[3]), "f"(q[4]), "f"(q[5]), "f"(q[6]), "f"(q[7]));
+  return r;
 }
 
 // RN(a / s) for an E4M3 block scale s > 0, given rcp = RN(1 / s): the product
@@ -124,13 +130,14 @@ __device__ __forceinline__ uint32_t quantize_block16(const float (&v)[16], float
   const uint32_t sf = f32_to_e4m3_satfinite(p6);
   const float s = e4m3_to_f32(sf);
   const float rcp = __frcp_rn(s);
-  uint32_t b[8];
+  float qa[8], qb[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j)
-    b[j] = e2m1x2(div_by_scale(__fmul_rn(v[2 * j], gs), s, rcp),
-                  div_by_scale(__fmul_rn(v[2 * j + 1], gs), s, rcp));
-  w0 = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
-  w1 = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
+  for (int i = 0; i < 8; ++i) {
+    qa[i] = div_by_scale(__fmul_rn(v[i], gs), s, rcp);
+    qb[i] = div_by_scale(__fmul_rn(v[8 + i], gs), s, rcp);
+  }
+  w0 = e2m1x8(qa);
+  w1 = e2m1x8(qb);
   return sf;
 }
 

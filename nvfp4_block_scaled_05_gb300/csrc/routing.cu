@@ -11,6 +11,7 @@
 //   3. scatter: per chunk, one warp walks the slots in order 32 at a time;
 //               __match_any_sync groups equal experts inside the warp, and
 //               the rank among lower lanes gives the stable position.
+// Up to kPermChunk slots, one block does all three (perm_single_kernel).
 #include "common.cuh"
 
 #include <mutex>
@@ -145,6 +146,73 @@ __global__ void __launch_bounds__(32) perm_scatter_kernel(const int32_t* __restr
   }
 }
 
+// n <= kPermChunk slots (decode-sized batches): the three steps in one block
+// of 1024 threads, the launch that dominates them at this size paid once: a
+// shared-memory histogram, the exclusive sum over experts (thread e owns
+// expert e), then warp 0 walks the slots in order as perm_scatter_kernel does.
+__global__ void __launch_bounds__(1024) perm_single_kernel(const int32_t* __restrict__ ids, int n, int E,
+                                                           int32_t* __restrict__ offsets,
+                                                           int32_t* __restrict__ perm_to_flat,
+                                                           int32_t* __restrict__ flat_to_perm) {
+  __shared__ int32_t next[1024];
+  __shared__ int32_t slot_e[kPermChunk];
+  __shared__ int32_t warp_sums[32];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  if (tid < E) next[tid] = 0;
+  __syncthreads();
+  if (tid < n) {
+    const int e = ids[tid];
+    slot_e[tid] = e;
+    atomicAdd(&next[e], 1);
+  }
+  __syncthreads();
+  const int total = tid < E ? next[tid] : 0;
+  int incl = total;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int y = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+    if (lane >= d) incl += y;
+  }
+  if (lane == 31) warp_sums[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    const int s = warp_sums[lane];
+    int si = s;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, si, d);
+      if (lane >= d) si += y;
+    }
+    warp_sums[lane] = si - s;
+  }
+  __syncthreads();
+  const int excl = warp_sums[wid] + incl - total;
+  if (tid < E) {
+    offsets[tid] = excl;
+    next[tid] = excl;
+  }
+  if (tid == 0) offsets[E] = n;
+  __syncthreads();
+  if (wid == 0) {
+    for (int i = 0; i < n; i += 32) {
+      const int f = i + lane;
+      const bool valid = f < n;
+      const int e = valid ? slot_e[f] : -1 - lane;  // invalid lanes never match a real expert
+      const uint32_t peers = __match_any_sync(0xFFFFFFFFu, e);
+      const int rank = __popc(peers & ((1u << lane) - 1u));
+      const int start = valid ? next[e] : 0;
+      __syncwarp();
+      if (valid) {
+        const int pos = start + rank;
+        perm_to_flat[pos] = f;
+        flat_to_perm[f] = pos;
+        if (lane == 31 - __clz(peers)) next[e] = start + __popc(peers);
+      }
+      __syncwarp();
+    }
+  }
+}
+
 constexpr int kCombineCols = 1024;   // columns per block: 128 threads x 8
 
 __global__ void __launch_bounds__(128) combine_kernel(const __nv_bfloat16* __restrict__ out,
@@ -223,6 +291,10 @@ extern "C" int moe_permute(const int32_t* topk_ids, int64_t T, int k, int E, int
   NVFP4_CHECK(ws && ws_bytes >= moe_permute_workspace_size(T, k, E) && aligned(ws, 16),
               NVFP4MOE_ERR_WORKSPACE);
   cudaStream_t s = as_stream(stream);
+  if (n <= kPermChunk) {
+    perm_single_kernel<<<1, 1024, 0, s>>>(topk_ids, (int)n, E, offsets, perm_to_flat, flat_to_perm);
+    return launch_status();
+  }
   const int nchunk = (int)ceil_div(n, kPermChunk);
   int32_t* counts = static_cast<int32_t*>(ws);
   if (nchunk > 0)
@@ -300,9 +372,13 @@ extern "C" int moe_permute_static_ws(const int32_t* topk_ids, int64_t T, int k, 
   NVFP4_CHECK(nchunk * E <= kStaticPermScratchInts, NVFP4MOE_ERR_WORKSPACE);
   NVFP4_CHECK(offsets, NVFP4MOE_ERR_INVALID);
   NVFP4_CHECK(n == 0 || (topk_ids && perm_to_flat && flat_to_perm), NVFP4MOE_ERR_INVALID);
+  cudaStream_t s = as_stream(stream);
+  if (n <= kPermChunk) {
+    perm_single_kernel<<<1, 1024, 0, s>>>(topk_ids, (int)n, E, offsets, perm_to_flat, flat_to_perm);
+    return launch_status();
+  }
   int32_t* counts = static_perm_scratch();
   NVFP4_CHECK(counts != nullptr, NVFP4MOE_ERR_LAUNCH);
-  cudaStream_t s = as_stream(stream);
   // every entry the scan reads is written by the count kernel first, so the
   // array needs no clearing between calls
   if (nchunk > 0)

@@ -31,8 +31,15 @@ if ROOT not in sys.path:
 METRIC = "MoE layer TFLOP/s & tokens/s at 1 GB300; % of FP4 tensor peak / HBM BW"
 FP4_OVER_BF16 = 13.5 / 2.25        # nominal dense FP4 / dense BF16 tensor rate
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNELS_PER_STEP = 10              # route 1, permute 3, quantize 3, L1 1, L2 1, combine 1
-KERNELS_PER_STEP_STATIC = 4        # fused dispatch 1, L1 1, L2 1, combine 1
+KERNELS_PER_STEP_FUSED = 4         # fused dispatch 1, L1 1, L2 1, combine 1 (static front too)
+
+
+def kernels_per_step(T, k, fused):
+    """Kernels of one moe_forward: the fused dispatch path, else route 1,
+    permute 1 (up to 1024 slots) or 3, quantize 3, L1 1, L2 1, combine 1."""
+    if fused:
+        return KERNELS_PER_STEP_FUSED
+    return 1 + (1 if T * k <= 1024 else 3) + 3 + 3
 
 
 def parse_args():
@@ -48,9 +55,11 @@ def parse_args():
     ap.add_argument("--cpu-experts", type=int, default=8,
                     help="experts whose routed rows form the CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--front", default="split", choices=["split", "static"],
-                    help="split: route/permute/quantize kernels with gs_x computed every step; "
-                         "static: moe_forward_static (one fused front kernel, gs_x pre-computed once)")
+    ap.add_argument("--front", default="dynamic", choices=["dynamic", "split", "static"],
+                    help="dynamic (or split): moe_forward, gs_x computed every step (one fused "
+                         "dispatch kernel when the tokens fit it, else route/permute/quantize "
+                         "kernels); static: moe_forward_static (one fused front kernel, gs_x "
+                         "pre-computed once)")
     ap.add_argument("--graph", action="store_true", help="replay the step as a captured CUDA graph")
     ap.add_argument("--op", default="moe", choices=["moe", "qnorm_rope", "linear"],
                     help="moe: the expert forward (default); qnorm_rope: the fused RMS norm + RoPE + "
@@ -475,7 +484,8 @@ def run_ours(args, cfg):
         raise RuntimeError("device status after timed region")
 
     # ---- per-stage device time (same stream, events between the six calls)
-    names = B.STATIC_STAGES if static else B.STAGES
+    fused_front = static or B.moe_forward_uses_fused_dispatch(T, E, k)
+    names = B.STATIC_STAGES if static else B.forward_stages(T, E, k)
     nst = len(names)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(args.steps)]
     barrier()
@@ -591,7 +601,9 @@ def run_ours(args, cfg):
                    "global_tokens": world * T, "parallelism": "replicas x%d" % world,
                    "active_experts": nums["active"], "seed": args.seed, "gs_h": cfg.gs_h,
                    "front": ("static (moe_forward_static; gs_x pre-computed once by a calibration "
-                             "forward)" if static else "split (gs_x computed every step)"),
+                             "forward)" if static else
+                             ("fused dispatch kernel (gs_x computed every step)" if fused_front else
+                              "route, permute and quantize kernels (gs_x computed every step)")),
                    "cuda_graph": bool(args.graph),
                    "l2": "inputs larger than L2: %.2f GB of expert weights streamed every step"
                          % (nums["bytes"] / 1e9)},
@@ -613,7 +625,7 @@ def run_ours(args, cfg):
                 "d2h_bytes_per_step": y.numel() * 2,
                 "copies": "pinned host <-> device every step, on their own streams, double-buffered "
                           "(overlapping the neighbouring steps' compute)"},
-        "gpu_launches": (KERNELS_PER_STEP_STATIC if static else KERNELS_PER_STEP) * args.steps,
+        "gpu_launches": kernels_per_step(T, k, fused_front) * args.steps,
         "clocks": clk,
     }
     if world == 1 and not args.no_cpu_baseline:

@@ -334,9 +334,13 @@ int moe_forward_workspace_layout(int64_t T, int64_t K, int64_t I, int E, int k,
  *   ws             >= moe_forward_workspace_size(T, K, I, E, k) bytes,
  *                  256-byte aligned.
  * Requires K % 128 == 0, I % 64 == 0, 1 <= k <= 16, k <= E <= 1024, T >= 0.
- * Enqueues route, permute, dispatch-quantize, L1+SwiGLU+requant, L2 and
- * combine kernels on `stream` without any host synchronisation, so the call
- * can be captured in a CUDA graph.
+ * Stages 1-2 run as moe_dispatch (one cooperative kernel) when
+ * moe_forward_uses_fused_dispatch(T, E, k), else as moe_route_topk,
+ * moe_permute and moe_quantize_dispatch; the intermediates are the same bit
+ * for bit. Then the
+ * L1+SwiGLU+requant, L2 and combine kernels. Everything is enqueued on
+ * `stream` without any host synchronisation, so the call can be captured in
+ * a CUDA graph.
  */
 int moe_forward(const void* x, const float* router_logits, int64_t T, int64_t K, int64_t I,
                 int E, int k, const uint8_t* w1_codes, const uint8_t* w1_sf,
@@ -344,7 +348,7 @@ int moe_forward(const void* x, const float* router_logits, int64_t T, int64_t K,
                 const float* gs_w2, const float* gs_h, void* y, void* ws, size_t ws_bytes,
                 void* stream);
 
-/* Workspace bytes moe_dispatch_static needs (T >= 1). */
+/* Workspace bytes moe_dispatch_static and moe_dispatch need (T >= 1). */
 size_t moe_dispatch_static_workspace_size(int64_t T, int E);
 
 /*
@@ -366,6 +370,31 @@ int moe_dispatch_static(const void* x, int64_t ldx, const float* router_logits, 
                         float* topk_w, int32_t* offsets, int32_t* perm_to_flat,
                         int32_t* flat_to_perm, uint8_t* a_codes, uint8_t* a_sf, int64_t a_rows,
                         void* ws, size_t ws_bytes, void* stream);
+
+/* 1 if T tokens at top-k over E experts fit the co-resident blocks of the
+ * fused dispatch kernel (moe_dispatch, moe_dispatch_static), else 0. Host
+ * only (queries the device's occupancy). */
+int moe_dispatch_supported(int64_t T, int E, int k);
+
+/* 1 if moe_forward runs stages 1-2 as moe_dispatch for this shape: when
+ * moe_dispatch_supported and T * k <= 65536 (above that the separate kernels
+ * are faster), else 0. Host only. */
+int moe_forward_uses_fused_dispatch(int64_t T, int E, int k);
+
+/*
+ * moe_dispatch -- moe_dispatch_static with the activation global scale
+ * computed in the same kernel (README "Bridge Layer": quantize_activation_nvfp4;
+ * CURRENT_BUG "What Works": recomputed every call): max |x| over all T tokens
+ * before the first grid barrier, gs = 2688 / max|x| (1 for an all-zero x)
+ * after it, written to *gs_out (device f32). Outputs, workspace
+ * (moe_dispatch_static_workspace_size) and requirements as
+ * moe_dispatch_static; the same bits as moe_route_topk + moe_permute +
+ * moe_quantize_dispatch with gs_in = NULL.
+ */
+int moe_dispatch(const void* x, int64_t ldx, const float* router_logits, int64_t T, int64_t K,
+                 int E, int k, float* gs_out, int32_t* topk_ids, float* topk_w, int32_t* offsets,
+                 int32_t* perm_to_flat, int32_t* flat_to_perm, uint8_t* a_codes, uint8_t* a_sf,
+                 int64_t a_rows, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * moe_forward_static -- moe_forward with a pre-computed activation global

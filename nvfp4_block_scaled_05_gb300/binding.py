@@ -59,6 +59,11 @@ _SIGS = {
     "moe_dispatch_static": (_int, [_c_void_p, _i64, _c_void_p, _i64, _i64, _int, _int, _c_void_p, _c_void_p,
                                    _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _i64,
                                    _c_void_p, _size, _c_void_p]),
+    "moe_dispatch_supported": (_int, [_i64, _int, _int]),
+    "moe_forward_uses_fused_dispatch": (_int, [_i64, _int, _int]),
+    "moe_dispatch": (_int, [_c_void_p, _i64, _c_void_p, _i64, _i64, _int, _int, _c_void_p, _c_void_p,
+                            _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _i64,
+                            _c_void_p, _size, _c_void_p]),
     "nvfp4_rmsnorm_rope_quantize": (_int, [_c_void_p, _i64, _i64, _i64, _c_void_p, ctypes.c_float, _i64,
                                            _c_void_p, _c_void_p, _c_void_p, _i64, _c_void_p, _c_void_p,
                                            _c_void_p, _int, _c_void_p, _c_void_p]),
@@ -381,15 +386,31 @@ def prepare_moe_weights(w1, w2, free_source=False):
     return out
 
 
-STAGES = ("route", "permute", "quantize", "l1_swiglu", "l2", "combine")
+SPLIT_STAGES = ("route", "permute", "quantize", "l1_swiglu", "l2", "combine")
+FUSED_STAGES = ("dispatch", "l1_swiglu", "l2", "combine")
 STATIC_STAGES = ("dispatch_static", "l1_swiglu", "l2", "combine")
 
 
+def moe_dispatch_supported(T, E, k):
+    return bool(lib().moe_dispatch_supported(T, E, k))
+
+
+def moe_forward_uses_fused_dispatch(T, E, k):
+    return bool(lib().moe_forward_uses_fused_dispatch(T, E, k))
+
+
+def forward_stages(T, E, k):
+    """The stages moe_forward runs for this shape: the fused dispatch kernel,
+    or the separate route, permute and quantize."""
+    return FUSED_STAGES if moe_forward_uses_fused_dispatch(T, E, k) else SPLIT_STAGES
+
+
 def moe_forward_stages(x, logits, weights, k, gs_h, ws, y, events=None):
-    """The six C calls moe_forward makes, issued one by one on the current
-    stream with the same workspace carving, so that CUDA events can be
-    recorded between them: events, if given, is a list of len(STAGES) + 1
-    torch.cuda.Event; events[i] is recorded before stage i."""
+    """The C calls moe_forward makes (forward_stages(T, E, k)), issued one by
+    one on the current stream with the same workspace carving, so that CUDA
+    events can be recorded between them: events, if given, is a list of
+    len(forward_stages(T, E, k)) + 1 torch.cuda.Event; events[i] is recorded
+    before stage i."""
     T, K = x.shape
     E = logits.shape[1]
     I = weights["I"]
@@ -411,28 +432,36 @@ def moe_forward_stages(x, logits, weights, k, gs_h, ws, y, events=None):
         if events is not None:
             events[i].record(st)
 
-    mark(0)
-    _check(L.moe_route_topk(_ptr(logits), T, E, k, p["topk_ids"], p["topk_w"], s), "route")
-    mark(1)
-    _check(L.moe_permute(p["topk_ids"], T, k, E, p["offsets"], p["perm_to_flat"], p["flat_to_perm"],
-                         ctypes.c_void_p(perm_ws), perm_bytes, s), "permute")
-    mark(2)
-    _check(L.moe_quantize_dispatch(_ptr(x), T, K, K, k, E, p["topk_ids"], p["offsets"], p["flat_to_perm"],
-                                   None, p["gs_x"], p["a_codes"], p["a_sf"], a_rows,
-                                   ctypes.c_void_p(disp_ws), disp_bytes, s), "quantize")
-    mark(3)
+    if moe_forward_uses_fused_dispatch(T, E, k):
+        mark(0)
+        _check(L.moe_dispatch(_ptr(x), K, _ptr(logits), T, K, E, k, p["gs_x"], p["topk_ids"], p["topk_w"],
+                              p["offsets"], p["perm_to_flat"], p["flat_to_perm"], p["a_codes"], p["a_sf"],
+                              a_rows, ctypes.c_void_p(perm_ws), ws.numel() - (perm_ws - base), s), "dispatch")
+        first = 1
+    else:
+        mark(0)
+        _check(L.moe_route_topk(_ptr(logits), T, E, k, p["topk_ids"], p["topk_w"], s), "route")
+        mark(1)
+        _check(L.moe_permute(p["topk_ids"], T, k, E, p["offsets"], p["perm_to_flat"], p["flat_to_perm"],
+                             ctypes.c_void_p(perm_ws), perm_bytes, s), "permute")
+        mark(2)
+        _check(L.moe_quantize_dispatch(_ptr(x), T, K, K, k, E, p["topk_ids"], p["offsets"], p["flat_to_perm"],
+                                       None, p["gs_x"], p["a_codes"], p["a_sf"], a_rows,
+                                       ctypes.c_void_p(disp_ws), disp_bytes, s), "quantize")
+        first = 3
+    mark(first)
     _check(L.nvfp4_grouped_gemm_swiglu(p["a_codes"], p["a_sf"], p["gs_x"], a_rows,
                                        _ptr(weights["w1_codes"]), _ptr(weights["w1_sf"]),
                                        _ptr(weights["gs_w1"]), p["offsets"], E, I, K, _ptr(gs_h),
                                        p["h_codes"], p["h_sf"], s), "l1_swiglu")
-    mark(4)
+    mark(first + 1)
     _check(L.nvfp4_grouped_gemm(p["h_codes"], p["h_sf"], _ptr(gs_h), a_rows, _ptr(weights["w2_codes"]),
                                 _ptr(weights["w2_sf"]), _ptr(weights["gs_w2"]), p["offsets"], E, K, I,
                                 p["out"], K, s), "l2")
-    mark(5)
+    mark(first + 2)
     _check(L.moe_combine(p["out"], K, p["topk_w"], p["flat_to_perm"], T, k, K, _ptr(y), y.stride(0), s),
            "combine")
-    mark(6)
+    mark(first + 3)
     return y
 
 

@@ -44,11 +44,15 @@ uint64_t wait_limit_ns();
 int device_num_sms();
 int test_stall_on();   // failure-path test hook (nvfp4moe_set_test_stall)
 
-// Fused front of moe_forward_static (front.cu).
+// Fused front (front.cu): routing, permutation, quantization and scatter in
+// one cooperative kernel; gs_x null = the global scale is computed from max|x|
+// (and written to gs_out when that is not null). moe_front_fits: whether T
+// tokens fit its co-resident blocks.
 size_t front_workspace_bytes(int64_t T, int E);
+bool moe_front_fits(int64_t T, int E, int k);
 int moe_front(const void* x, int64_t ldx, const float* logits, int64_t T, int64_t K, int E, int k,
-              const float* gs_x, int32_t* ids, float* w, int32_t* offsets, int32_t* p2f, int32_t* f2p,
-              uint8_t* a_codes, uint8_t* a_sf, void* ws, size_t ws_bytes, cudaStream_t s);
+              const float* gs_x, float* gs_out, int32_t* ids, float* w, int32_t* offsets, int32_t* p2f,
+              int32_t* f2p, uint8_t* a_codes, uint8_t* a_sf, void* ws, size_t ws_bytes, cudaStream_t s);
 
 // Byte offset of the scale of (row r, 16-element block b) in the tiled layout
 // documented in nvfp4moe.h.

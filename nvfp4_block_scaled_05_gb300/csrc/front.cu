@@ -1,13 +1,14 @@
-// Fused front of the MoE forward with a pre-computed activation global scale
-// ("NVFP4 MegaMoE Kernel" README, "Bridge Layer": quantize_activation_nvfp4,
-// the CUDA-graph-safe quantizer with a pre-computed gs; "MoE Runner" steps 1
-// and 2): routing, the stable permutation, NVFP4 quantization and the scatter
-// into the padded L1 operand, in one cooperative launch.
+// Fused front of the MoE forward ("NVFP4 MegaMoE Kernel" README, "MoE Runner"
+// steps 1 and 2; "Bridge Layer": quantize_activation_nvfp4, with a
+// pre-computed gs on the CUDA-graph-safe path, else the global scale of x
+// computed here): routing, the stable permutation, NVFP4 quantization and the
+// scatter into the padded L1 operand, in one cooperative launch.
 //
 // G blocks; block c owns the contiguous tokens [c*tpb, (c+1)*tpb) and so the
 // contiguous flat slots [c*tpb*k, (c+1)*tpb*k).
 //   phase 1  route the block's tokens (one warp per token) and histogram
-//            their experts -> counts[c][e]
+//            their experts -> counts[c][e]; without a pre-computed gs, also
+//            max |x| over the block's rows -> one atomicMax
 //   -- grid barrier --
 //   phase 2  block c turns the columns e = c, c+G, ... into exclusive prefixes
 //            over blocks (counts[c'][e] = slots of expert e in blocks < c'),
@@ -17,7 +18,8 @@
 //            writes them) and padded group starts; the stable position of
 //            each of its slots (one warp, 32 slots at a time, grouped with
 //            __match_any_sync), then each token row is quantized once and
-//            written to the padded rows of its k slots.
+//            written to the padded rows of its k slots (gs = 2688 / max|x|
+//            when it was not given).
 // The same permutation as moe_permute (a stable counting sort by expert of
 // the flat slots t*k + j), the same rows as moe_quantize_dispatch.
 //
@@ -40,7 +42,9 @@ struct FrontParams {
   const float* logits;
   int64_t T;
   int K, E, k, tpb;
-  const float* gs_x;
+  const float* gs_x;       // pre-computed global scale, or null: computed from max|x|
+  float* gs_out;           // null, or receives the global scale used
+  uint32_t* amax_bits;     // max|x| as f32 bits (zeroed before the launch)
   int32_t* ids;
   float* w;
   int32_t* offsets;
@@ -150,8 +154,41 @@ __global__ void __launch_bounds__(kFrontThreads) moe_front_kernel(const FrontPar
       atomicAdd(&next[my_i], 1);
     }
   }
+  if (!p.gs_x) {
+    // max |x| over the block's rows, four 16-byte loads in flight per thread
+    const int vpr = p.K / 8;
+    const int nvec = ntok * vpr;
+    float m = 0.0f;
+    for (int i0 = tid; i0 < nvec; i0 += 4 * kFrontThreads) {
+      uint4 u[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int i = i0 + j * kFrontThreads;
+        u[j] = make_uint4(0u, 0u, 0u, 0u);
+        if (i < nvec) {
+          const int tl = i / vpr;
+          u[j] = __ldg(reinterpret_cast<const uint4*>(p.x + (t0 + tl) * p.ldx) + (i - tl * vpr));
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float f[8];
+        bf16x8_to_f32(u[j], f);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) m = fmaxf(m, fabsf(f[q]));
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if (lane == 0) misc[warp] = (int32_t)__float_as_uint(m);
+  }
   __syncthreads();
   for (int e = tid; e < E; e += kFrontThreads) p.counts[(int64_t)c * E + e] = next[e];
+  if (!p.gs_x && tid == 0) {
+    uint32_t mb = 0;
+    for (int i = 0; i < nwarps; ++i) mb = max(mb, (uint32_t)misc[i]);   // non-negative f32 bits order as floats
+    if (mb > 0) atomicMax(p.amax_bits, mb);
+  }
   if (p.test_stall && c == 0) return;
   if (!grid_barrier(p, (unsigned)G, 8, misc + 31)) return;
 
@@ -203,7 +240,8 @@ __global__ void __launch_bounds__(kFrontThreads) moe_front_kernel(const FrontPar
     }
   }
   __syncthreads();
-  const float gs = *p.gs_x;
+  const float gs = p.gs_x ? *p.gs_x : global_scale_from_amax_bits(__ldcg(p.amax_bits));
+  if (p.gs_out && c == 0 && tid == 0) *p.gs_out = gs;
   const int nchunk = (p.K + 511) / 512;
   const int64_t c4 = p.K / 64;
   for (int item = warp; item < ntok * nchunk; item += nwarps) {
@@ -271,9 +309,22 @@ size_t front_workspace_bytes(int64_t T, int E) {
   return 256 + (size_t)ceil_div((int64_t)E * 4, 256) * 256 + (size_t)ceil_div(g * E * 4, 256) * 256;
 }
 
+bool moe_front_fits(int64_t T, int E, int k) {
+  if (T < 1 || k < 1 || k > 16 || k > E || E > 1024) return false;
+  const size_t smem_max = front_smem_bytes(E, kFrontMaxSlots);
+  const int vpl = vpl_of(E);
+  int gmax = vpl == 1 ? max_coresident<1>(smem_max) : vpl == 2 ? max_coresident<2>(smem_max)
+           : vpl == 4 ? max_coresident<4>(smem_max) : vpl == 8 ? max_coresident<8>(smem_max)
+           : vpl == 16 ? max_coresident<16>(smem_max) : max_coresident<32>(smem_max);
+  if (gmax > kFrontMaxBlocks) gmax = kFrontMaxBlocks;
+  if (gmax < 1) return false;
+  const int64_t G = T < gmax ? T : gmax;
+  return ceil_div(T, G) * k <= kFrontMaxSlots;
+}
+
 int moe_front(const void* x, int64_t ldx, const float* logits, int64_t T, int64_t K, int E, int k,
-              const float* gs_x, int32_t* ids, float* w, int32_t* offsets, int32_t* p2f, int32_t* f2p,
-              uint8_t* a_codes, uint8_t* a_sf, void* ws, size_t ws_bytes, cudaStream_t s) {
+              const float* gs_x, float* gs_out, int32_t* ids, float* w, int32_t* offsets, int32_t* p2f,
+              int32_t* f2p, uint8_t* a_codes, uint8_t* a_sf, void* ws, size_t ws_bytes, cudaStream_t s) {
   NVFP4_CHECK(T >= 1 && K % 64 == 0 && k >= 1 && k <= 16 && k <= E && E <= 1024, NVFP4MOE_ERR_UNSUPPORTED);
   NVFP4_CHECK(ws && ws_bytes >= front_workspace_bytes(T, E) && aligned(ws, 256), NVFP4MOE_ERR_WORKSPACE);
   const size_t smem_max = front_smem_bytes(E, kFrontMaxSlots);
@@ -297,6 +348,7 @@ int moe_front(const void* x, int64_t ldx, const float* logits, int64_t T, int64_
   p.k = k;
   p.tpb = tpb;
   p.gs_x = gs_x;
+  p.gs_out = gs_out;
   p.ids = ids;
   p.w = w;
   p.offsets = offsets;
@@ -306,13 +358,14 @@ int moe_front(const void* x, int64_t ldx, const float* logits, int64_t T, int64_
   p.a_sf = a_sf;
   uint8_t* wb = static_cast<uint8_t*>(ws);
   p.barrier = reinterpret_cast<unsigned int*>(wb);
+  p.amax_bits = reinterpret_cast<uint32_t*>(wb + 4);
   p.totals = reinterpret_cast<int32_t*>(wb + 256);
   p.counts = reinterpret_cast<int32_t*>(wb + 256 + ceil_div((int64_t)E * 4, 256) * 256);
   p.limit_ns = wait_limit_ns();
   p.status = device_status_word();
   p.test_stall = test_stall_on();
   NVFP4_CHECK(p.status, NVFP4MOE_ERR_LAUNCH);
-  if (cudaMemsetAsync(p.barrier, 0, sizeof(unsigned int), s) != cudaSuccess) return NVFP4MOE_ERR_LAUNCH;
+  if (cudaMemsetAsync(p.barrier, 0, 2 * sizeof(unsigned int), s) != cudaSuccess) return NVFP4MOE_ERR_LAUNCH;
   const size_t smem = front_smem_bytes(E, tpb * k);
   switch (vpl) {
     case 1: return launch_front_vpl<1>(p, G, smem, s);

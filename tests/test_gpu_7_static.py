@@ -154,3 +154,80 @@ def test_static_graph_replay_on_new_inputs():
         eager = B.moe_forward_static(src["x"], src["logits"], wts, cfg.k, gs_h, gs_x)
         assert B.nvfp4moe_last_device_status() == 0
         assert torch.equal(y_s, eager)
+
+
+def _split_and_fused(cfg, x, logits):
+    """Stages 1-2 of the forward twice into two workspaces of moe_forward's
+    layout: as the separate route, permute and quantize calls, and as the
+    fused dispatch kernel with the global scale computed in it."""
+    import ctypes
+    T, K, I, E, k = cfg.T, cfg.K, cfg.I, cfg.E, cfg.k
+    L = B.lib()
+    nb = B.moe_forward_workspace_size(T, K, I, E, k)
+    lay = B.moe_forward_workspace_layout(T, K, I, E, k)
+    a_rows = lay["a_rows"]
+    up = lambda v: -(-v // 256) * 256
+    out = []
+    for fused in (False, True):
+        ws = torch.full((nb,), 0xAB, dtype=torch.uint8, device=DEV)   # stale bytes
+        base = ws.data_ptr()
+        p = {n: ctypes.c_void_p(base + o) for n, o in lay.items() if n != "a_rows"}
+        scratch = base + lay["out"] + up(T * k * K * 2)
+        s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        xp, lp = ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(logits.data_ptr())
+        if fused:
+            st = L.moe_dispatch(xp, K, lp, T, K, E, k, p["gs_x"], p["topk_ids"], p["topk_w"], p["offsets"],
+                                p["perm_to_flat"], p["flat_to_perm"], p["a_codes"], p["a_sf"], a_rows,
+                                ctypes.c_void_p(scratch), nb - (scratch - base), s)
+            assert st == 0, st
+        else:
+            pb = int(L.moe_permute_workspace_size(T, k, E))
+            assert L.moe_route_topk(lp, T, E, k, p["topk_ids"], p["topk_w"], s) == 0
+            assert L.moe_permute(p["topk_ids"], T, k, E, p["offsets"], p["perm_to_flat"], p["flat_to_perm"],
+                                 ctypes.c_void_p(scratch), pb, s) == 0
+            dws = scratch + up(pb)
+            assert L.moe_quantize_dispatch(xp, T, K, K, k, E, p["topk_ids"], p["offsets"], p["flat_to_perm"],
+                                           None, p["gs_x"], p["a_codes"], p["a_sf"], a_rows,
+                                           ctypes.c_void_p(dws), int(L.moe_quantize_dispatch_workspace_size(E)),
+                                           s) == 0
+        assert B.nvfp4moe_last_device_status() == 0
+        d = _inter(ws, lay, T, K, E, k)
+        d["gs_x"] = _view(ws, lay, "gs_x", torch.float32, 1).item()
+        out.append(d)
+    return out
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "prefill", "skewed", "dsv4_decode"])
+def test_fused_dispatch_equals_separate_calls(name):
+    """moe_dispatch (one cooperative kernel, the global scale of x computed in
+    it) writes the same bits as moe_route_topk + moe_permute +
+    moe_quantize_dispatch: routing, permutation, offsets, gs_x, and every
+    routed row's codes and scales."""
+    cfg = W.CONFIGS[name]
+    assert B.moe_dispatch_supported(cfg.T, cfg.E, cfg.k)
+    inp = W.moe_inputs(cfg, seed=5, device=DEV, weights=False)
+    split, fused = _split_and_fused(cfg, inp["x"], inp["logits"])
+    assert fused["gs_x"] == split["gs_x"]
+    for n in NAMES + ["rows", "sf"]:
+        assert np.array_equal(fused[n], split[n]), n
+
+
+def test_fused_dispatch_edge_shapes():
+    """T=1; more experts than routed rows (E=1000); every token on one expert;
+    an all-zero x (global scale 1)."""
+    for (T, K, E, k, mode) in [(1, 256, 8, 2, "rand"), (3, 384, 1000, 4, "rand"), (200, 256, 4, 1, "one"),
+                               (64, 512, 16, 2, "zero")]:
+        cfg = W.MoEConfig("edge", T=T, K=K, I=64, E=E, k=k, gs_h=336.0)
+        g = torch.Generator(device="cpu").manual_seed(T + E)
+        x = torch.randn(T, K, generator=g).to(torch.bfloat16)
+        if mode == "zero":
+            x.zero_()
+        logits = torch.randn(T, E, generator=g)
+        if mode == "one":
+            logits[:, 2] += 100.0
+        split, fused = _split_and_fused(cfg, x.to(DEV), logits.to(DEV))
+        assert fused["gs_x"] == split["gs_x"], (T, E)
+        if mode == "zero":
+            assert fused["gs_x"] == 1.0
+        for n in NAMES + ["rows", "sf"]:
+            assert np.array_equal(fused[n], split[n]), (n, T, E)

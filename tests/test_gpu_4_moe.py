@@ -146,3 +146,34 @@ def test_moe_deterministic_and_graph_capturable():
     torch.cuda.synchronize()
     assert torch.equal(y1, y3)
     assert B.nvfp4moe_last_device_status() == 0
+
+
+def test_moe_largest_expert_count_and_topk():
+    """E=1024 experts with top-16 (the largest the entry points accept) and
+    E=1024 with top-1, against the oracle for every token."""
+    for (T, K, I, E, k) in [(8, 256, 64, 1024, 16), (40, 128, 64, 1024, 1)]:
+        cfg = W.MoEConfig("max", T=T, K=K, I=I, E=E, k=k, gs_h=336.0)
+        g = torch.Generator(device="cpu").manual_seed(E + k)
+        x = torch.randn(T, K, generator=g).to(torch.bfloat16)
+        logits = torch.randn(T, E, generator=g)
+        w1 = (torch.randn(E, 2 * I, K, generator=g) * 0.05).to(torch.bfloat16)
+        w2 = (torch.randn(E, K, I, generator=g) * 0.05).to(torch.bfloat16)
+        wts = B.prepare_moe_weights(w1.to(DEV), w2.to(DEV))
+        gs_h = torch.tensor([cfg.gs_h], dtype=torch.float32, device=DEV)
+        y = B.moe_forward(x.to(DEV), logits.to(DEV), wts, k, gs_h)
+        assert B.nvfp4moe_last_device_status() == 0
+        xb, w1b, w2b = W.bf16_bits(x), W.bf16_bits(w1), W.bf16_bits(w2)
+        ref = O.moe_forward(xb, logits.numpy(), lambda e: w1b[e], lambda e: w2b[e], k, np.float32(cfg.gs_h))
+        got = y.float().cpu().numpy()
+        assert_close_tol(got, ref["y"], "E=%d k=%d" % (E, k))
+        assert cosine(got, ref["y"]) >= 0.9995
+
+
+def test_fused_dispatch_choice():
+    """moe_forward takes the fused dispatch kernel up to 65536 routed rows and
+    the separate kernels above."""
+    assert B.moe_forward_uses_fused_dispatch(128, 256, 8)
+    assert B.moe_forward_uses_fused_dispatch(8192, 256, 8)
+    assert not B.moe_forward_uses_fused_dispatch(8193, 256, 8)
+    assert not B.moe_forward_uses_fused_dispatch(16384, 256, 8)
+    assert B.moe_dispatch_supported(16384, 256, 8)

@@ -44,7 +44,7 @@ def _check(guards, inputs, before):
         assert torch.equal(t, c), "input changed: " + name
 
 
-@pytest.mark.parametrize("front", ["split", "static"])
+@pytest.mark.parametrize("front", ["dynamic", "static"])
 def test_forward_writes_only_its_outputs(front):
     cfg = W.MoEConfig("canary", T=300, K=1024, I=384, E=24, k=4, gs_h=336.0)
     inp = W.moe_inputs(cfg, seed=8, device=DEV)
@@ -56,7 +56,7 @@ def test_forward_writes_only_its_outputs(front):
     inputs = {"x": inp["x"], "logits": inp["logits"], "gs_h": gs_h,
               **{n: wts[n] for n in ["w1_codes", "w1_sf", "gs_w1", "w2_codes", "w2_sf", "gs_w2"]}}
     before = [t.clone() for t in inputs.values()]
-    if front == "split":
+    if front == "dynamic":
         out = B.moe_forward(inp["x"], inp["logits"], wts, k, gs_h, ws=ws.bytes(), y=y.view(torch.bfloat16, (T, K)))
     else:
         gs_x = torch.tensor([300.0], device=DEV)
@@ -150,3 +150,30 @@ def test_permute_and_combine_write_only_their_outputs():
     y = Guarded(T * K * 2)
     B.moe_combine(out, w, f2p.view(torch.int32, (T * k,)), y=y.view(torch.bfloat16, (T, K)))
     _check({"y": y}, {"out": out, "w": w}, [out.clone(), w.clone()])
+
+
+def test_route_and_quantize_dispatch_write_only_their_outputs():
+    """The separate stage-1/2 kernels moe_forward uses above 65536 routed rows:
+    routing, then the quantize + scatter into padded rows (with the global
+    scale computed), each into guarded outputs."""
+    T, K, E, k = 513, 1024, 40, 6
+    g = torch.Generator(device="cpu").manual_seed(12)
+    x = torch.randn(T, K, generator=g).to(torch.bfloat16).to(DEV)
+    logits = torch.randn(T, E, generator=g).to(DEV)
+    ids = Guarded(T * k * 4)
+    w = Guarded(T * k * 4)
+    L = B.lib()
+    assert L.moe_route_topk(B._ptr(logits), T, E, k, B._ptr(ids.bytes()), B._ptr(w.bytes()), B._stream()) == 0
+    _check({"ids": ids, "w": w}, {"logits": logits}, [logits.clone()])
+    offsets, p2f, f2p = B.moe_permute(ids.view(torch.int32, (T, k)), E)
+    a_rows = B.nvfp4moe_padded_rows(T * k, E)
+    codes = Guarded(a_rows * K // 2)
+    sf = Guarded(B.nvfp4_sf_bytes(a_rows, K))
+    gs = Guarded(4)
+    ws = Guarded(int(L.moe_quantize_dispatch_workspace_size(E)))
+    inputs = {"x": x, "offsets": offsets, "f2p": f2p}
+    before = [t.clone() for t in inputs.values()]
+    assert L.moe_quantize_dispatch(B._ptr(x), T, K, K, k, E, B._ptr(ids.bytes()), B._ptr(offsets), B._ptr(f2p),
+                                   None, B._ptr(gs.bytes()), B._ptr(codes.bytes()), B._ptr(sf.bytes()), a_rows,
+                                   B._ptr(ws.bytes()), ws.n, B._stream()) == 0
+    _check({"codes": codes, "sf": sf, "gs": gs, "ws": ws}, inputs, before)

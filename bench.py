@@ -768,14 +768,14 @@ def run_linear(args):
     wc, wsf, gsw = B.nvfp4_quantize(inp["w"][0])
     a_rows = -(-M // 128) * 128
     xc = torch.zeros((a_rows, K // 2), dtype=torch.uint8, device=dev)
-    xsf = torch.zeros(B.nvfp4_sf_bytes(a_rows, K), dtype=torch.uint8, device=dev)
+    xsf = torch.zeros(B.nvfp4_sf_bytes(a_rows, K, B.NVFP4_SF_TILED_ROWS), dtype=torch.uint8, device=dev)
     gsx = torch.empty(1, device=dev)
     out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
     lws = torch.empty(int(B.lib().nvfp4_linear_workspace_size()), dtype=torch.uint8, device=dev)
     flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
     def fn():
-        B.nvfp4_quantize(x, codes=xc[:M], sf=xsf, gs_out=gsx)
+        B.nvfp4_quantize(x, codes=xc[:M], sf=xsf, gs_out=gsx, sf_layout=B.NVFP4_SF_TILED_ROWS)
         B.nvfp4_linear(xc, xsf, gsx, M, wc, wsf, gsw, out=out, ws=lws)
     for _ in range(args.warmup):
         fn()
@@ -804,7 +804,7 @@ def run_linear(args):
 
     def e2e_step():
         x_d.copy_(x_h, non_blocking=True)
-        B.nvfp4_quantize(x_d, codes=xc[:M], sf=xsf, gs_out=gsx)
+        B.nvfp4_quantize(x_d, codes=xc[:M], sf=xsf, gs_out=gsx, sf_layout=B.NVFP4_SF_TILED_ROWS)
         B.nvfp4_linear(xc, xsf, gsx, M, wc, wsf, gsw, out=out, ws=lws)
         o_h.copy_(out, non_blocking=True)
     e2e_step()

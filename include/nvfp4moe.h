@@ -42,6 +42,16 @@
  *       of 4; the scale of row r, 16-element block b lives at byte
  *         ((r / 128) * C4 + b / 4) * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4 + b % 4
  *       with C4 = ceil(cols / 64). Size: nvfp4_sf_bytes(rows, cols, TILED).
+ *       The grouped GEMMs read their weight (B) scales in this layout.
+ *     NVFP4_SF_TILED_ROWS: tiles of 128 rows x 16 scale columns (2048 bytes),
+ *       row-major inside: the scale of row r, block b lives at byte
+ *         ((r / 128) * S + b / 16) * 2048 + (r % 128) * 16 + b % 16
+ *       with S = ceil(cols / 256); rows padded to 128, scale columns to 16.
+ *       The grouped GEMMs read their activation (A) scales in this layout:
+ *       one 256-element K stage of 128 rows is 2048 contiguous bytes, and a
+ *       row's 16 consecutive blocks are 16 contiguous bytes, so a quantizer
+ *       that scatters rows writes whole 16-byte pieces. Size:
+ *       nvfp4_sf_bytes(rows, cols, TILED_ROWS).
  * - Quantization rule (README "Correctness Bugs Fixed", bugs 3 and 4): per
  *   block, p = amax * gs; a block with amax == 0 or p < 6 * 2^-9 gets scale
  *   byte 0 and all codes 0; otherwise sf = E4M3_rn_satfinite(p / 6) and
@@ -89,6 +99,7 @@ enum {
 
 #define NVFP4_SF_ROWMAJOR 0
 #define NVFP4_SF_TILED 1
+#define NVFP4_SF_TILED_ROWS 2
 
 /* Short description of a status code (static string). */
 const char* nvfp4moe_status_string(int status);
@@ -124,9 +135,9 @@ size_t nvfp4_quantize_workspace_size(void);
  *            `rows` entries: output row r reads x row row_src[r]; a negative
  *            entry makes output row r all-zero (codes 0, scales 0).
  *   codes    rows x cols/2 bytes (output, 8-byte aligned).
- *   sf       scales (output) in layout sf_layout (NVFP4_SF_ROWMAJOR or
- *            NVFP4_SF_TILED); in the tiled layout the padding rows/columns
- *            are not written.
+ *   sf       scales (output) in layout sf_layout (NVFP4_SF_ROWMAJOR,
+ *            NVFP4_SF_TILED or NVFP4_SF_TILED_ROWS); in the tiled layouts
+ *            the padding rows/columns are not written.
  *   ws       when gs_in == NULL: >= nvfp4_quantize_workspace_size() bytes,
  *            16-byte aligned; otherwise ignored (may be NULL).
  * Errors: INVALID (null pointer, cols % 16 != 0, misalignment, bad layout),
@@ -198,7 +209,7 @@ size_t moe_quantize_dispatch_workspace_size(int E);
  * P_e + (flat_to_perm[f] - offsets[e]).
  *   gs_in / gs_out as in nvfp4_quantize (gs_in == NULL: gs = 2688 / amax(x),
  *   recomputed every call, CURRENT_BUG.md "What Works").
- *   a_codes  a_rows x K/2 bytes, a_sf NVFP4_SF_TILED for (a_rows, K);
+ *   a_codes  a_rows x K/2 bytes, a_sf NVFP4_SF_TILED_ROWS for (a_rows, K);
  *   a_rows >= nvfp4moe_padded_rows(T*k, E). Padding rows are not written.
  * K must be a multiple of 64.
  */
@@ -212,7 +223,7 @@ int moe_quantize_dispatch(const void* x, int64_t T, int64_t K, int64_t ldx, int 
  * nvfp4_grouped_gemm -- README "ScaledGroupedGemmKernel": A(M, K) x B(E, K, N)
  * -> C(M, N), block-scaled on both operands, per-expert global scales.
  *   A        grouped-padded NVFP4 activation: a_codes a_rows x K/2, a_sf
- *            NVFP4_SF_TILED for (a_rows, K), global scale *gs_a.
+ *            NVFP4_SF_TILED_ROWS for (a_rows, K), global scale *gs_a.
  *   B        expert weights (E, N, K) as described above, gs_b[E].
  *   offsets  (E + 1) int32 group boundaries (compact rows).
  *   C        BF16, COMPACT rows: C[offsets[e] + i, n] =
@@ -237,9 +248,9 @@ int nvfp4_grouped_gemm(const uint8_t* a_codes, const uint8_t* a_sf, const float*
  * quantize_activation_nvfp4 with pre-computed gs; "Fused SwiGLU - Remaining
  * Steps" 2-4: quantize in the epilogue and store FP4 + scales straight into
  * the padded L2 input).
- *   h_codes  a_rows x I/2 bytes (32-byte aligned), h_sf NVFP4_SF_TILED for
- *            (a_rows, I), in the same grouped-padded rows as A (padding rows
- *            are not written).
+ *   h_codes  a_rows x I/2 bytes (32-byte aligned), h_sf NVFP4_SF_TILED_ROWS
+ *            for (a_rows, I), in the same grouped-padded rows as A (padding
+ *            rows are not written): the A operand of the L2 GEMM.
  * Requires I % 64 == 0, K % 64 == 0, 1 <= E <= 1024.
  */
 int nvfp4_grouped_gemm_swiglu(const uint8_t* a_codes, const uint8_t* a_sf, const float* gs_a,
@@ -264,7 +275,8 @@ int nvfp4_grouped_gemm_swiglu(const uint8_t* a_codes, const uint8_t* a_sf, const
  *   cos_tab, sin_tab  (max_pos, rope_dims / 2) f32, row-major (device,
  *              16-byte aligned).
  *              With rope_dims == 0 positions and tables are not read.
- *   codes      (rows, D/2) bytes; sf in NVFP4_SF_ROWMAJOR or NVFP4_SF_TILED.
+ *   codes      (rows, D/2) bytes; sf in NVFP4_SF_ROWMAJOR, NVFP4_SF_TILED or
+ *              NVFP4_SF_TILED_ROWS.
  *   y_out      NULL, or (rows, D) f32 that receives y (16-byte aligned).
  * Requires D % 16 == 0, rope_dims % 16 == 0, rope_dims <= D.
  */
@@ -286,7 +298,7 @@ size_t nvfp4_linear_workspace_size(void);
  * with one group, so it can run on its own stream beside the routed experts.
  *   A   a_rows x K/2 codes, row-major (nvfp4_quantize output), with
  *       a_rows >= 128 * ceil(M / 128) allocated rows (rows >= M are read and
- *       their products discarded), scales NVFP4_SF_TILED for (a_rows, K),
+ *       their products discarded), scales NVFP4_SF_TILED_ROWS for (a_rows, K),
  *       global scale *gs_a (device).
  *   W   N x K/2 codes, scales NVFP4_SF_TILED for (N, K), *gs_w (device).
  *   C   M x N BF16, leading dimension ldc (alignment as nvfp4_grouped_gemm).

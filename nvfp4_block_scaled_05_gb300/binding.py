@@ -14,7 +14,8 @@ import torch
 from . import build as _build
 
 NVFP4_SF_ROWMAJOR = 0
-NVFP4_SF_TILED = 1
+NVFP4_SF_TILED = 1          # weight (B) operand scales of the GEMMs
+NVFP4_SF_TILED_ROWS = 2     # activation (A) operand scales of the GEMMs
 
 _c_void_p = ctypes.c_void_p
 _i64 = ctypes.c_int64
@@ -237,7 +238,7 @@ def moe_quantize_dispatch(x, topk_ids, offsets, flat_to_perm, E, gs=None, a_rows
     if a_rows is None:
         a_rows = nvfp4moe_padded_rows(T * k, E)
     a_codes = torch.zeros((a_rows, K // 2), dtype=torch.uint8, device=dev)
-    a_sf = torch.zeros(nvfp4_sf_bytes(a_rows, K), dtype=torch.uint8, device=dev)
+    a_sf = torch.zeros(nvfp4_sf_bytes(a_rows, K, NVFP4_SF_TILED_ROWS), dtype=torch.uint8, device=dev)
     gs_out = torch.empty(1, dtype=torch.float32, device=dev)
     nb = int(lib().moe_quantize_dispatch_workspace_size(E))
     ws = torch.empty(nb, dtype=torch.uint8, device=dev)
@@ -305,7 +306,7 @@ def nvfp4_grouped_gemm_swiglu(a_codes, a_sf, gs_a, w1_codes, w1_sf, gs_w1, offse
     if h_codes is None:
         h_codes = torch.zeros((a_rows, I // 2), dtype=torch.uint8, device=dev)
     if h_sf is None:
-        h_sf = torch.zeros(nvfp4_sf_bytes(a_rows, I), dtype=torch.uint8, device=dev)
+        h_sf = torch.zeros(nvfp4_sf_bytes(a_rows, I, NVFP4_SF_TILED_ROWS), dtype=torch.uint8, device=dev)
     _check(lib().nvfp4_grouped_gemm_swiglu(_ptr(a_codes), _ptr(a_sf), _ptr(gs_a), a_rows,
                                            _ptr(w1_codes), _ptr(w1_sf), _ptr(gs_w1), _ptr(offsets), E,
                                            I, K, _ptr(gs_h), _ptr(h_codes), _ptr(h_sf), _stream()),

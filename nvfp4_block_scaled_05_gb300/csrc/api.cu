@@ -21,6 +21,7 @@ extern "C" size_t nvfp4_sf_bytes(int64_t rows, int64_t cols, int sf_layout) {
   if (rows < 0 || cols < 0) return 0;
   if (sf_layout == NVFP4_SF_ROWMAJOR) return (size_t)(rows * (cols / 16));
   if (sf_layout == NVFP4_SF_TILED) return (size_t)(ceil_div(rows, 128) * ceil_div(cols, 64) * 512);
+  if (sf_layout == NVFP4_SF_TILED_ROWS) return (size_t)(ceil_div(rows, 128) * ceil_div(cols, 256) * 2048);
   return 0;
 }
 
@@ -70,9 +71,9 @@ Layout make_layout(int64_t T, int64_t K, int64_t I, int E, int k) {
   L.off[4] = take(M * 4);
   L.off[5] = take(4);
   L.off[6] = take(a_rows * (K / 2));
-  L.off[7] = take((int64_t)nvfp4_sf_bytes(a_rows, K, NVFP4_SF_TILED));
+  L.off[7] = take((int64_t)nvfp4_sf_bytes(a_rows, K, NVFP4_SF_TILED_ROWS));
   L.off[8] = take(a_rows * (I / 2));
-  L.off[9] = take((int64_t)nvfp4_sf_bytes(a_rows, I, NVFP4_SF_TILED));
+  L.off[9] = take((int64_t)nvfp4_sf_bytes(a_rows, I, NVFP4_SF_TILED_ROWS));
   L.off[10] = take(M * K * 2);
   L.off[11] = a_rows;
   // scratch: the permute and dispatch workspaces (moe_forward), or the fused

@@ -65,6 +65,15 @@ __host__ __device__ inline int64_t sf_tiled_offset(int64_t r, int64_t b, int64_t
   return sf_tiled_row_part(r, c4) + sf_tiled_block_part(b);
 }
 
+// The same for NVFP4_SF_TILED_ROWS, the layout of the GEMMs' activation (A)
+// scales: tiles of 128 rows x 16 blocks (2048 bytes), row-major inside; s =
+// ceil(cols / 256) tiles per 128 rows.
+__host__ __device__ inline int64_t sf_rows_row_part(int64_t r, int64_t s) { return (r >> 7) * s * 2048 + (r & 127) * 16; }
+__host__ __device__ inline int64_t sf_rows_block_part(int64_t b) { return (b >> 4) * 2048 + (b & 15); }
+__host__ __device__ inline int64_t sf_rows_offset(int64_t r, int64_t b, int64_t s) {
+  return sf_rows_row_part(r, s) + sf_rows_block_part(b);
+}
+
 // ------------------------------------------------------------------ NVFP4 encode
 
 // Exact value of an E4M3 byte (every E4M3 value is representable in f16).

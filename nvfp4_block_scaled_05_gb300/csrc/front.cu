@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(kFrontThreads) moe_front_kernel(const FrontPar
   const float gs = p.gs_x ? *p.gs_x : global_scale_from_amax_bits(__ldcg(p.amax_bits));
   if (p.gs_out && c == 0 && tid == 0) *p.gs_out = gs;
   const int nchunk = (p.K + 511) / 512;
-  const int64_t c4 = p.K / 64;
+  const int64_t s_tiles = (p.K + 255) / 256;
   for (int item = warp; item < ntok * nchunk; item += nwarps) {
     const int tl = item / nchunk;
     const int64_t col0 = (int64_t)(item - tl * nchunk) * 512 + lane * 16;
@@ -255,12 +255,12 @@ __global__ void __launch_bounds__(kFrontThreads) moe_front_kernel(const FrontPar
       const int e = slot_e[tl * k + lane];
       const int64_t prow = (int64_t)pad[e] + slot_pos[tl * k + lane] - offs[e];
       my_codes = reinterpret_cast<unsigned long long>(p.a_codes + prow * (p.K / 2));
-      my_sf = reinterpret_cast<unsigned long long>(p.a_sf + sf_tiled_row_part(prow, c4));
+      my_sf = reinterpret_cast<unsigned long long>(p.a_sf + sf_rows_row_part(prow, s_tiles));
     }
     uint32_t w0 = 0, w1 = 0, s = 0;
     if (valid) s = quantize_lane16(p.x + (t0 + tl) * p.ldx, col0, gs, w0, w1);
     const uint32_t word = gather_sf_word(s);
-    const int64_t code_col = col0 / 2, sf_col = sf_tiled_block_part(col0 / 16);
+    const int64_t code_col = col0 / 2, sf_col = sf_rows_block_part(col0 / 16);
     for (int j = 0; j < k; ++j) {
       uint8_t* dc = reinterpret_cast<uint8_t*>(__shfl_sync(0xFFFFFFFFu, my_codes, j));
       uint8_t* ds = reinterpret_cast<uint8_t*>(__shfl_sync(0xFFFFFFFFu, my_sf, j));

@@ -89,7 +89,8 @@ struct Params {
   int E;
   int N;
   int K;
-  int64_t sf_rowtile_bytes;   // (K/64) * 512: scale bytes of 128 rows
+  int64_t sf_rowtile_bytes;   // (K/64) * 512: weight scale bytes of 128 rows (NVFP4_SF_TILED)
+  int64_t a_sf_rowtile_bytes; // ceil(K/256) * 2048: activation scale bytes of 128 rows (TILED_ROWS)
   int64_t b_sf_expert_bytes;  // scale bytes of one expert's N x K weights
   // plain epilogue
   __nv_bfloat16* c;
@@ -271,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       c.a_row = pad_off[e] + mb * BM;
       c.b_row = e * p.N + nb * BN;
       c.bhalves = ncols / 128;
-      c.sfa = p.a_sf + (int64_t)(c.a_row / BM) * p.sf_rowtile_bytes;
+      c.sfa = p.a_sf + (int64_t)(c.a_row / BM) * p.a_sf_rowtile_bytes;
       c.sfb = p.b_sf + (int64_t)e * p.b_sf_expert_bytes + (int64_t)(nb * 2) * p.sf_rowtile_bytes;
       return c;
     };
@@ -291,8 +292,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int nk = min(4, ksteps - kb * 4);
           const uint32_t sffull = bar_sffull + 8 * stage;
           const uint32_t sdst = sbase + OFF_SF + stage * SF_BYTES;
-          mbar_arrive_expect_tx(sffull, (1 + cur.bhalves) * nk * 512);
-          bulk_load(sdst, cur.sfa + kb * 2048, nk * 512, sffull, pol_a);
+          // the activation scales of a stage are 2048 bytes whatever the K tail
+          mbar_arrive_expect_tx(sffull, 2048 + cur.bhalves * nk * 512);
+          bulk_load(sdst, cur.sfa + kb * 2048, 2048, sffull, pol_a);
           for (int h = 0; h < cur.bhalves; ++h)
             bulk_load(sdst + SFA_BYTES + h * SFA_BYTES, cur.sfb + h * p.sf_rowtile_bytes + kb * 2048, nk * 512,
                       sffull, pol_w);
@@ -339,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto load_tile = [&](int t) {
       int e, nb, mb, rows, ncols;
       sch.decode(t, e, nb, mb, rows, ncols);
-      csfa = p.a_sf + (int64_t)((pad_off[e] + mb * BM) / BM) * p.sf_rowtile_bytes;
+      csfa = p.a_sf + (int64_t)((pad_off[e] + mb * BM) / BM) * p.a_sf_rowtile_bytes;
       csfb = p.b_sf + (int64_t)e * p.b_sf_expert_bytes + (int64_t)(nb * 2) * p.sf_rowtile_bytes;
       ctwo = ncols > 128;
     };
@@ -353,12 +355,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         return false;
       const int nk = min(4, ksteps - ckb * 4);
       const uint32_t dst = sbase + OFF_SF + slot * SF_BYTES;
-      // 384 chunks of 16 bytes: SFA atoms (128), then SFB halves 0 and 1 (128 each);
-      // chunks past a K tail, or of a missing second half, are not copied
+      // 384 chunks of 16 bytes: the activation scales (128 rows x 16 bytes),
+      // then the weight scale atoms of halves 0 and 1 (128 each); weight atoms
+      // past a K tail, or of a missing second half, are not copied
 #pragma unroll
       for (int i = 0; i < 3; ++i) {
         const int c = st_id + kScaleThreads * i;           // region i, chunk st_id
-        const bool live = st_id < nk * 32 && (i < 2 || ctwo);
+        const bool live = i == 0 || (st_id < nk * 32 && (i < 2 || ctwo));
         if (live) {
           const uint8_t* src = i == 0 ? csfa + ckb * 2048 + st_id * 16
                                       : csfb + (int64_t)(i - 1) * p.sf_rowtile_bytes + ckb * 2048 + st_id * 16;
@@ -384,16 +387,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         p.wait_limit_ns, p.status, 5);
       ok = __all_sync(0xFFFFFFFFu, ok);
       if (!ok) break;
-      // Atom layout: 16-byte chunk `lane` of a 512-byte atom holds rows lane,
-      // lane+32, lane+64, lane+96 (4 bytes each, one per 16-element block); the
-      // word of row 32q + lane is word q. Slots past a K tail (and the second
+      // Activation scales: row r's 16 blocks are the 16 bytes at r * 16, the
+      // word of k-step kk at r * 16 + 4 kk. Weight atoms: 16-byte chunk `lane`
+      // of a 512-byte atom holds rows lane, lane+32, lane+64, lane+96 (4 bytes
+      // each, one per 16-element block). Slots past a K tail (and the second
       // half of a 128-column tile) hold stale bytes the MMAs never read.
-      const uint8_t* ssfa = smem + OFF_SF + slot * SF_BYTES + lane * 16 + q * 4;
+      const uint8_t* ssfa = smem + OFF_SF + slot * SF_BYTES + (q * 32 + lane) * 16;
       const uint8_t* ssfb = smem + OFF_SF + slot * SF_BYTES + SFA_BYTES + lane * 16;
       uint32_t a[4], b[32];
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
-        a[kk] = *reinterpret_cast<const uint32_t*>(ssfa + kk * 512);    // row 32q + lane
+        a[kk] = *reinterpret_cast<const uint32_t*>(ssfa + kk * 4);      // row 32q + lane
         // B rows lane+32j, j = 0..3 (first 128 rows) and 4..7 (second 128 rows)
         const uint4 lo = *reinterpret_cast<const uint4*>(ssfb + kk * 512);
         const uint4 hi = *reinterpret_cast<const uint4*>(ssfb + SFA_BYTES + kk * 512);
@@ -581,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         uint8_t* hc = p.h_codes + hrow * (p.I / 2) + hfeat / 2;   // 32-byte aligned (I % 64 == 0)
         st_global_32B(hc, words[0], words[1], words[2], words[3], words[4], words[5], words[6], words[7]);
-        *reinterpret_cast<uint32_t*>(p.h_sf + sf_tiled_offset(hrow, hfeat / 16, p.I / 64)) = sfw;
+        *reinterpret_cast<uint32_t*>(p.h_sf + sf_rows_offset(hrow, hfeat / 16, (p.I + 255) / 256)) = sfw;
       }
     }
   }
@@ -717,6 +721,7 @@ extern "C" int nvfp4_grouped_gemm(const uint8_t* a_codes, const uint8_t* a_sf, c
   p.N = (int)N;
   p.K = (int)K;
   p.sf_rowtile_bytes = (K / 64) * 512;
+  p.a_sf_rowtile_bytes = ((K + 255) / 256) * 2048;
   p.b_sf_expert_bytes = (int64_t)nvfp4_sf_bytes(N, K, NVFP4_SF_TILED);
   p.c = static_cast<__nv_bfloat16*>(c);
   p.ldc = ldc;
@@ -743,6 +748,7 @@ extern "C" int nvfp4_grouped_gemm_swiglu(const uint8_t* a_codes, const uint8_t* 
   p.N = (int)(2 * I);
   p.K = (int)K;
   p.sf_rowtile_bytes = (K / 64) * 512;
+  p.a_sf_rowtile_bytes = ((K + 255) / 256) * 2048;
   p.b_sf_expert_bytes = (int64_t)nvfp4_sf_bytes(2 * I, K, NVFP4_SF_TILED);
   p.h_codes = h_codes;
   p.h_sf = h_sf;

@@ -82,6 +82,10 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(
     const uint32_t word = gather_sf_word(s);
     if (valid && (lane & 3) == 0)
       *reinterpret_cast<uint32_t*>(sf + sf_tiled_offset(r, col0 / 16, (cols + 63) / 64)) = word;
+  } else if (sf_layout == NVFP4_SF_TILED_ROWS) {
+    const uint32_t word = gather_sf_word(s);
+    if (valid && (lane & 3) == 0)
+      *reinterpret_cast<uint32_t*>(sf + sf_rows_offset(r, col0 / 16, (cols + 255) / 256)) = word;
   } else if (valid) {
     sf[r * (cols / 16) + col0 / 16] = static_cast<uint8_t>(s);
   }
@@ -127,19 +131,19 @@ __global__ void __launch_bounds__(256) dispatch_quantize_kernel(
   // lane j < k finds the padded row of slot j while the row is being quantized,
   // and the row parts of its code and scale addresses (the warp's lanes then
   // only add their column parts)
-  const int64_t c4 = K / 64;
+  const int64_t s_tiles = (K + 255) / 256;
   unsigned long long my_codes = 0, my_sf = 0;
   if (lane < k) {
     const int64_t f = t * k + lane;
     const int e = topk_ids[f];
     const int64_t prow = pad_off[e] + flat_to_perm[f] - offsets[e];
     my_codes = reinterpret_cast<unsigned long long>(a_codes + prow * (K / 2));
-    my_sf = reinterpret_cast<unsigned long long>(a_sf + sf_tiled_row_part(prow, c4));
+    my_sf = reinterpret_cast<unsigned long long>(a_sf + sf_rows_row_part(prow, s_tiles));
   }
   uint32_t w0 = 0, w1 = 0, s = 0;
   if (valid) s = quantize_lane16(x + t * ldx, col0, gs, w0, w1);
   const uint32_t word = gather_sf_word(s);
-  const int64_t code_col = col0 / 2, sf_col = sf_tiled_block_part(col0 / 16);
+  const int64_t code_col = col0 / 2, sf_col = sf_rows_block_part(col0 / 16);
   for (int j = 0; j < k; ++j) {
     uint8_t* dc = reinterpret_cast<uint8_t*>(__shfl_sync(0xFFFFFFFFu, my_codes, j));
     uint8_t* ds = reinterpret_cast<uint8_t*>(__shfl_sync(0xFFFFFFFFu, my_sf, j));
@@ -238,14 +242,15 @@ __device__ __forceinline__ uint32_t norm_rope_store(const NormRopeArgs& a, int64
 __device__ __forceinline__ void norm_rope_store_sf(const NormRopeArgs& a, int64_t r, int64_t b, uint32_t sfb,
                                                    uint32_t word, bool words) {
   const int64_t nb = a.D / 16;
+  auto offset = [&](int64_t bb) {
+    return a.sf_layout == NVFP4_SF_TILED        ? sf_tiled_offset(r, bb, (a.D + 63) / 64)
+           : a.sf_layout == NVFP4_SF_TILED_ROWS ? sf_rows_offset(r, bb, (a.D + 255) / 256)
+                                                : r * nb + bb;
+  };
   if (words) {
-    if ((b & 3) == 0) {
-      const int64_t off = a.sf_layout == NVFP4_SF_TILED ? sf_tiled_offset(r, b, (a.D + 63) / 64) : r * nb + b;
-      *reinterpret_cast<uint32_t*>(a.sf + off) = word;
-    }
+    if ((b & 3) == 0) *reinterpret_cast<uint32_t*>(a.sf + offset(b)) = word;
   } else {
-    const int64_t off = a.sf_layout == NVFP4_SF_TILED ? sf_tiled_offset(r, b, (a.D + 63) / 64) : r * nb + b;
-    a.sf[off] = static_cast<uint8_t>(sfb);
+    a.sf[offset(b)] = static_cast<uint8_t>(sfb);
   }
 }
 
@@ -396,7 +401,8 @@ extern "C" int nvfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t
                               uint8_t* codes, uint8_t* sf, int sf_layout, void* ws,
                               size_t ws_bytes, void* stream) {
   NVFP4_CHECK(rows >= 0 && cols >= 0 && cols % 16 == 0, NVFP4MOE_ERR_INVALID);
-  NVFP4_CHECK(sf_layout == NVFP4_SF_ROWMAJOR || sf_layout == NVFP4_SF_TILED, NVFP4MOE_ERR_INVALID);
+  NVFP4_CHECK(sf_layout == NVFP4_SF_ROWMAJOR || sf_layout == NVFP4_SF_TILED || sf_layout == NVFP4_SF_TILED_ROWS,
+              NVFP4MOE_ERR_INVALID);
   if (rows == 0 || cols == 0) return NVFP4MOE_OK;
   NVFP4_CHECK(x && codes && sf, NVFP4MOE_ERR_INVALID);
   NVFP4_CHECK(ldx >= cols && ldx % 8 == 0 && aligned(x, 16) && aligned(codes, 8), NVFP4MOE_ERR_INVALID);
@@ -453,7 +459,8 @@ extern "C" int nvfp4_rmsnorm_rope_quantize(const void* x, int64_t rows, int64_t 
                                            void* stream) {
   NVFP4_CHECK(rows >= 0 && D > 0 && D % 16 == 0 && rope_dims >= 0 && rope_dims % 16 == 0 && rope_dims <= D,
               NVFP4MOE_ERR_UNSUPPORTED);
-  NVFP4_CHECK(sf_layout == NVFP4_SF_ROWMAJOR || sf_layout == NVFP4_SF_TILED, NVFP4MOE_ERR_INVALID);
+  NVFP4_CHECK(sf_layout == NVFP4_SF_ROWMAJOR || sf_layout == NVFP4_SF_TILED || sf_layout == NVFP4_SF_TILED_ROWS,
+              NVFP4MOE_ERR_INVALID);
   if (rows == 0) return NVFP4MOE_OK;
   NVFP4_CHECK(x && gamma && gs && codes && sf && eps >= 0.0f, NVFP4MOE_ERR_INVALID);
   NVFP4_CHECK(rope_dims == 0 || (positions && cos_tab && sin_tab && max_pos > 0), NVFP4MOE_ERR_INVALID);

@@ -17,6 +17,20 @@ def sf_tiled_to_rowmajor(sf_tiled, rows, cols):
     return sf[sf_tiled_index(rows, cols)]
 
 
+def sf_rows_index(rows, cols):
+    """Byte index in the NVFP4_SF_TILED_ROWS layout (the GEMMs' activation
+    scales) of every (r, b) scale, as (rows, cols//16)."""
+    r = np.arange(rows, dtype=np.int64)[:, None]
+    b = np.arange(cols // 16, dtype=np.int64)[None, :]
+    s = (cols + 255) // 256
+    return ((r // 128) * s + b // 16) * 2048 + (r % 128) * 16 + b % 16
+
+
+def sf_rows_to_rowmajor(sf_rows, rows, cols):
+    sf = np.asarray(sf_rows).reshape(-1)
+    return sf[sf_rows_index(rows, cols)]
+
+
 def padded_starts(offsets):
     """P_e = 128 * sum_{e'<e} ceil(n_e'/128)."""
     offsets = np.asarray(offsets, np.int64)

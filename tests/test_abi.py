@@ -41,6 +41,10 @@ def test_host_only_entry_points(lib):
     assert B.nvfp4_sf_bytes(128, 64, B.NVFP4_SF_TILED) == 512
     assert B.nvfp4_sf_bytes(129, 65, B.NVFP4_SF_TILED) == 2 * 2 * 512
     assert B.nvfp4_sf_bytes(3, 32, B.NVFP4_SF_ROWMAJOR) == 6
+    assert B.nvfp4_sf_bytes(128, 256, B.NVFP4_SF_TILED_ROWS) == 2048
+    assert B.nvfp4_sf_bytes(129, 257 // 16 * 16, B.NVFP4_SF_TILED_ROWS) == 2 * 1 * 2048
+    assert B.nvfp4_sf_bytes(128, 7168, B.NVFP4_SF_TILED_ROWS) == B.nvfp4_sf_bytes(128, 7168, B.NVFP4_SF_TILED)
+    assert B.nvfp4_sf_bytes(256, 320, B.NVFP4_SF_TILED_ROWS) == 2 * 2 * 2048
     assert B.nvfp4moe_padded_rows(1024, 256) == -(-(1024 + 256 * 127) // 128) * 128
     assert B.nvfp4moe_padded_rows(1000, 3) == -(-(1000 + 3 * 127) // 128) * 128
     assert B.nvfp4moe_padded_rows(1, 8) == 128

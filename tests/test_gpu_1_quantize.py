@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import oracle as O
-from helpers import sf_tiled_to_rowmajor, padded_rows_of_compact
+from helpers import sf_rows_to_rowmajor, sf_tiled_to_rowmajor, padded_rows_of_compact
 from nvfp4_block_scaled_05_gb300 import binding as B
 from nvfp4_block_scaled_05_gb300 import workloads as W
 
@@ -26,6 +26,7 @@ def _quant_check(x, gs_given=None, layout=B.NVFP4_SF_TILED):
     got_c = codes.cpu().numpy()
     got_s = sf.cpu().numpy()
     got_s = (sf_tiled_to_rowmajor(got_s, rows, cols) if layout == B.NVFP4_SF_TILED
+             else sf_rows_to_rowmajor(got_s, rows, cols) if layout == B.NVFP4_SF_TILED_ROWS
              else got_s.reshape(rows, cols // 16))
     assert np.array_equal(got_s, rs), "scale bytes differ at %s" % (np.argwhere(got_s != rs)[:5],)
     bad = np.argwhere(got_c != rc)
@@ -37,6 +38,14 @@ def _quant_check(x, gs_given=None, layout=B.NVFP4_SF_TILED):
 def test_quantize_random_tiled():
     g = torch.Generator().manual_seed(11)
     _quant_check(torch.randn(300, 1024, generator=g).to(torch.bfloat16))
+
+
+def test_quantize_activation_layout_and_ragged_cols():
+    """The GEMMs' activation scale layout (NVFP4_SF_TILED_ROWS), with row and
+    column counts that leave partial 128-row and 256-column tiles."""
+    g = torch.Generator().manual_seed(14)
+    _quant_check(torch.randn(300, 1024, generator=g).to(torch.bfloat16), layout=B.NVFP4_SF_TILED_ROWS)
+    _quant_check(torch.randn(129, 592, generator=g).to(torch.bfloat16), layout=B.NVFP4_SF_TILED_ROWS)
 
 
 def test_quantize_rowmajor_and_ragged_cols():
@@ -131,7 +140,7 @@ def test_dispatch_quantize_padded_rows_bit_exact():
     rc, rs = O.quantize_bf16(xb, gs_ref)
     prow = padded_rows_of_compact(offsets)
     a_rows = a_codes.shape[0]
-    gsf = sf_tiled_to_rowmajor(a_sf.cpu().numpy(), a_rows, cfg.K)
+    gsf = sf_rows_to_rowmajor(a_sf.cpu().numpy(), a_rows, cfg.K)
     gc = a_codes.cpu().numpy()
     for r in range(cfg.M):
         t = p2f[r] // cfg.k

@@ -14,7 +14,7 @@ import torch
 
 import oracle as O
 from helpers import (assert_close_tol, cosine, padded_rows_of_compact, padded_starts,
-                     sf_tiled_index)
+                     sf_rows_index, sf_tiled_index)
 from nvfp4_block_scaled_05_gb300 import binding as B
 
 pytestmark = pytest.mark.gpu
@@ -28,10 +28,20 @@ def _dump(name, **arrays):
 
 
 def _tile_sf(sf_rm, rows_cap, cols):
-    """Row-major (rows, cols/16) scales -> tiled bytes of a (rows_cap, cols) matrix."""
+    """Row-major (rows, cols/16) scales -> tiled bytes of a (rows_cap, cols) matrix
+    (the weight operand's layout)."""
     out = np.zeros(B.nvfp4_sf_bytes(rows_cap, cols), np.uint8)
     rows = sf_rm.shape[0]
     out[sf_tiled_index(rows, cols)] = sf_rm
+    return out
+
+
+def _rows_sf(sf_rm, rows_cap, cols):
+    """Row-major (rows, cols/16) scales -> NVFP4_SF_TILED_ROWS bytes of a
+    (rows_cap, cols) matrix (the activation operand's layout)."""
+    out = np.zeros(B.nvfp4_sf_bytes(rows_cap, cols, B.NVFP4_SF_TILED_ROWS), np.uint8)
+    rows = sf_rm.shape[0]
+    out[sf_rows_index(rows, cols)] = sf_rm
     return out
 
 
@@ -72,7 +82,7 @@ def _run_grouped(rng, counts, N, K, mode_a="random", mode_b="random", name="g", 
     asf_rm = np.zeros((a_rows, K // 16), np.uint8)
     asf_rm[prow] = asf
     d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
-    a_sf_t = _tile_sf(asf_rm, a_rows, K)
+    a_sf_t = _rows_sf(asf_rm, a_rows, K)
     b_sf_t = np.concatenate([_tile_sf(bsf[e], N, K) for e in range(E)])
     out = None
     if wide:
@@ -129,7 +139,7 @@ def test_linear_workload_sampled_rows():
     from nvfp4_block_scaled_05_gb300 import workloads as W
     cfg = W.CONFIGS["linear"]
     inp = W.linear_inputs(cfg, seed=0, device=DEV)
-    xq, xsf, gsx = B.nvfp4_quantize(inp["x"])
+    xq, xsf, gsx = B.nvfp4_quantize(inp["x"], sf_layout=B.NVFP4_SF_TILED_ROWS)
     wq, wsf, gsw = B.nvfp4_quantize(inp["w"][0])
     offsets = torch.tensor([0, cfg.M], dtype=torch.int32, device=DEV)
     c = B.nvfp4_grouped_gemm(xq, xsf, gsx, wq.view(1, cfg.N, cfg.K // 2), wsf, gsw, offsets)
@@ -187,12 +197,12 @@ def test_swiglu_epilogue_against_oracle_requant():
     w1c = np.stack([O.interleave_rows(w[0], 8) for w in w1])
     w1s = np.concatenate([_tile_sf(O.interleave_rows(w[1], 8), 2 * I, K) for w in w1])
     gsw = np.array([w[2] for w in w1], np.float32)
-    h_codes, h_sf = B.nvfp4_grouped_gemm_swiglu(d(a_pad), d(_tile_sf(asf_rm, a_rows, K)),
+    h_codes, h_sf = B.nvfp4_grouped_gemm_swiglu(d(a_pad), d(_rows_sf(asf_rm, a_rows, K)),
                                                 d(np.array([gsa], np.float32)), d(w1c), d(w1s), d(gsw),
                                                 d(offsets), d(np.array([gs_h], np.float32)))
     assert B.nvfp4moe_last_device_status() == 0
     gc = h_codes.cpu().numpy()[prow]
-    gs_rm = h_sf.cpu().numpy()[sf_tiled_index(a_rows, I)][prow]
+    gs_rm = h_sf.cpu().numpy()[sf_rows_index(a_rows, I)][prow]
     sf_mismatch = np.mean(gs_rm != hs_ref)
     code_mismatch = np.mean(gc != hc_ref)
     hd_gpu = O.dequantize_f64(gc, gs_rm, gs_h)

@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import oracle as O
-from helpers import (assert_close_tol, cosine, padded_rows_of_compact, sf_tiled_index)
+from helpers import (assert_close_tol, cosine, padded_rows_of_compact, sf_rows_index)
 from nvfp4_block_scaled_05_gb300 import binding as B
 from nvfp4_block_scaled_05_gb300 import workloads as W
 
@@ -53,11 +53,11 @@ def _run(cfg, seed, sample):
     assert _ws_view(ws, lay, "gs_x", torch.float32, 1).item() == ref["gs_x"]
     a_rows = lay["a_rows"]
     a_codes = _ws_view(ws, lay, "a_codes", torch.uint8, a_rows * K // 2).view(a_rows, K // 2)
-    a_sf = _ws_view(ws, lay, "a_sf", torch.uint8, B.nvfp4_sf_bytes(a_rows, K)).cpu().numpy()
+    a_sf = _ws_view(ws, lay, "a_sf", torch.uint8, B.nvfp4_sf_bytes(a_rows, K, B.NVFP4_SF_TILED_ROWS)).cpu().numpy()
     prow = padded_rows_of_compact(offsets)
     # every routed copy of the sampled tokens carries that token's quantized row
     f2p = ref["flat_to_perm"]
-    sf_idx = sf_tiled_index(a_rows, K)
+    sf_idx = sf_rows_index(a_rows, K)
     for ti, t in enumerate(ref["tokens"]):
         for j in range(k):
             p = prow[f2p[t * k + j]]

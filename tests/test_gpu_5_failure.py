@@ -22,7 +22,7 @@ def _operands():
     offsets = torch.arange(0, M + 1, per, dtype=torch.int32).to(DEV)
     a_rows = B.nvfp4moe_padded_rows(M, E)
     a_codes = torch.randint(0, 256, (a_rows, K // 2), dtype=torch.uint8, generator=g).to(DEV)
-    a_sf = torch.full((B.nvfp4_sf_bytes(a_rows, K),), 0x38, dtype=torch.uint8, device=DEV)
+    a_sf = torch.full((B.nvfp4_sf_bytes(a_rows, K, B.NVFP4_SF_TILED_ROWS),), 0x38, dtype=torch.uint8, device=DEV)
     b_codes = torch.randint(0, 256, (E, N, K // 2), dtype=torch.uint8, generator=g).to(DEV)
     b_sf = torch.full((E * B.nvfp4_sf_bytes(N, K),), 0x38, dtype=torch.uint8, device=DEV)
     one = torch.ones(1, device=DEV)

@@ -20,8 +20,8 @@ def _quantize_padded(x):
     M, K = x.shape
     a_rows = max(128, -(-M // 128) * 128)
     codes = torch.zeros((a_rows, K // 2), dtype=torch.uint8, device=x.device)
-    sf = torch.zeros(B.nvfp4_sf_bytes(a_rows, K), dtype=torch.uint8, device=x.device)
-    _, _, gs = B.nvfp4_quantize(x, codes=codes[:M], sf=sf)
+    sf = torch.zeros(B.nvfp4_sf_bytes(a_rows, K, B.NVFP4_SF_TILED_ROWS), dtype=torch.uint8, device=x.device)
+    _, _, gs = B.nvfp4_quantize(x, codes=codes[:M], sf=sf, sf_layout=B.NVFP4_SF_TILED_ROWS)
     return codes, sf, gs
 
 

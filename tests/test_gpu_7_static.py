@@ -15,7 +15,7 @@ import pytest
 import torch
 
 import oracle as O
-from helpers import assert_close_tol, cosine, padded_rows_of_compact, sf_tiled_index
+from helpers import assert_close_tol, cosine, padded_rows_of_compact, sf_rows_index
 from nvfp4_block_scaled_05_gb300 import binding as B
 from nvfp4_block_scaled_05_gb300 import workloads as W
 
@@ -37,9 +37,9 @@ def _inter(ws, lay, T, K, E, k):
     a_rows = lay["a_rows"]
     prow = padded_rows_of_compact(d["offsets"])
     codes = _view(ws, lay, "a_codes", torch.uint8, a_rows * K // 2).view(a_rows, K // 2).cpu().numpy()
-    sf = _view(ws, lay, "a_sf", torch.uint8, B.nvfp4_sf_bytes(a_rows, K)).cpu().numpy()
+    sf = _view(ws, lay, "a_sf", torch.uint8, B.nvfp4_sf_bytes(a_rows, K, B.NVFP4_SF_TILED_ROWS)).cpu().numpy()
     d["rows"] = codes[prow]
-    d["sf"] = sf[sf_tiled_index(a_rows, K)][prow]
+    d["sf"] = sf[sf_rows_index(a_rows, K)][prow]
     return d
 
 

@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import oracle as O
-from helpers import cosine, sf_tiled_index
+from helpers import cosine, sf_rows_index, sf_tiled_index
 from nvfp4_block_scaled_05_gb300 import binding as B
 from nvfp4_block_scaled_05_gb300 import workloads as W
 
@@ -30,7 +30,8 @@ def _inputs(rows, D, R, P, seed):
 
 
 @pytest.mark.parametrize("rows,D,R,layout", [(300, 192, 64, B.NVFP4_SF_TILED), (257, 576, 64, B.NVFP4_SF_ROWMAJOR),
-                                             (37, 7168, 0, B.NVFP4_SF_TILED), (1, 64, 64, B.NVFP4_SF_TILED)])
+                                             (37, 7168, 0, B.NVFP4_SF_TILED), (1, 64, 64, B.NVFP4_SF_TILED),
+                                             (300, 192, 64, B.NVFP4_SF_TILED_ROWS)])
 def test_norm_rope_quantize_matches_oracle(rows, D, R, layout):
     P = 4096
     x, gamma, cos_t, sin_t, pos = _inputs(rows, D, R, P, rows + D)
@@ -50,7 +51,9 @@ def test_norm_rope_quantize_matches_oracle(rows, D, R, layout):
     assert np.all(np.abs(yg - yref) <= 1e-5 * np.abs(yref) + 1e-6 * scale)
     c = codes.cpu().numpy()
     s = sf.cpu().numpy()
-    s_rm = s[sf_tiled_index(rows, D)] if layout == B.NVFP4_SF_TILED else s.reshape(rows, D // 16)
+    s_rm = (s[sf_tiled_index(rows, D)] if layout == B.NVFP4_SF_TILED
+            else s[sf_rows_index(rows, D)] if layout == B.NVFP4_SF_TILED_ROWS
+            else s.reshape(rows, D // 16))
     c_own, s_own = O.quantize_f32(yg, gs)
     assert np.array_equal(c, c_own) and np.array_equal(s_rm, s_own)
     c_ref, s_ref = O.quantize_f32(yref.astype(np.float32), gs)

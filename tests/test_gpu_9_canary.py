@@ -76,10 +76,10 @@ def test_quantize_gemm_linear_norm_write_only_their_outputs():
     # quantize (rows not a multiple of 128, tiled scales)
     a_rows = B.nvfp4moe_padded_rows(M, E)
     codes = Guarded(a_rows * K // 2, fill=0)
-    sf = Guarded(B.nvfp4_sf_bytes(a_rows, K), fill=0)
+    sf = Guarded(B.nvfp4_sf_bytes(a_rows, K, B.NVFP4_SF_TILED_ROWS), fill=0)
     gs = Guarded(4)
     B.nvfp4_quantize(x, codes=codes.view(torch.uint8, (a_rows, K // 2))[:M], sf=sf.view(torch.uint8, (-1,)),
-                     gs_out=gs.view(torch.float32, (1,)))
+                     gs_out=gs.view(torch.float32, (1,)), sf_layout=B.NVFP4_SF_TILED_ROWS)
     _check({"codes": codes, "sf": sf, "gs": gs}, {"x": x}, [x_in])
     # grouped GEMM (groups of 100, 0, 233 rows in the padded layout) and the SwiGLU GEMM
     I = N // 2
@@ -88,11 +88,12 @@ def test_quantize_gemm_linear_norm_write_only_their_outputs():
     wq = B.prepare_moe_weights(w1, w2)
     offsets = torch.tensor([0, 100, 100, M], dtype=torch.int32, device=DEV)
     a_codes = torch.zeros((a_rows, K // 2), dtype=torch.uint8, device=DEV)
-    a_sf = torch.zeros(B.nvfp4_sf_bytes(a_rows, K), dtype=torch.uint8, device=DEV)
+    a_sf = torch.zeros(B.nvfp4_sf_bytes(a_rows, K, B.NVFP4_SF_TILED_ROWS), dtype=torch.uint8, device=DEV)
     row_src = torch.full((a_rows,), -1, dtype=torch.int32, device=DEV)
     row_src[:100] = torch.arange(0, 100, dtype=torch.int32, device=DEV)          # group 0 at padded row 0
     row_src[128:128 + 233] = torch.arange(100, M, dtype=torch.int32, device=DEV)  # group 2 at padded row 128
-    B.nvfp4_quantize(x, row_src=row_src, codes=a_codes, sf=a_sf, gs_out=gs.view(torch.float32, (1,)))
+    B.nvfp4_quantize(x, row_src=row_src, codes=a_codes, sf=a_sf, gs_out=gs.view(torch.float32, (1,)),
+                     sf_layout=B.NVFP4_SF_TILED_ROWS)
     gsx = gs.view(torch.float32, (1,)).clone()
     c = Guarded(M * N * 2)
     ins = {"a_codes": a_codes, "a_sf": a_sf, "w1_codes": wq["w1_codes"], "offsets": offsets}
@@ -101,7 +102,7 @@ def test_quantize_gemm_linear_norm_write_only_their_outputs():
                          out=c.view(torch.bfloat16, (M, N)))
     _check({"c": c}, ins, before)
     hc = Guarded(a_rows * I // 2, fill=0)
-    hs = Guarded(B.nvfp4_sf_bytes(a_rows, I), fill=0)
+    hs = Guarded(B.nvfp4_sf_bytes(a_rows, I, B.NVFP4_SF_TILED_ROWS), fill=0)
     gs_h = torch.tensor([200.0], device=DEV)
     B.nvfp4_grouped_gemm_swiglu(a_codes, a_sf, gsx, wq["w1_codes"], wq["w1_sf"], wq["gs_w1"], offsets, gs_h,
                                 h_codes=hc.view(torch.uint8, (a_rows, I // 2)), h_sf=hs.view(torch.uint8, (-1,)))
@@ -110,8 +111,8 @@ def test_quantize_gemm_linear_norm_write_only_their_outputs():
     lin = Guarded(M * (N + 8) * 2)
     lws = Guarded(int(B.lib().nvfp4_linear_workspace_size()))
     xq = torch.zeros((-(-M // 128) * 128, K // 2), dtype=torch.uint8, device=DEV)
-    xs = torch.zeros(B.nvfp4_sf_bytes(xq.shape[0], K), dtype=torch.uint8, device=DEV)
-    B.nvfp4_quantize(x, codes=xq[:M], sf=xs, gs_out=gs.view(torch.float32, (1,)))
+    xs = torch.zeros(B.nvfp4_sf_bytes(xq.shape[0], K, B.NVFP4_SF_TILED_ROWS), dtype=torch.uint8, device=DEV)
+    B.nvfp4_quantize(x, codes=xq[:M], sf=xs, gs_out=gs.view(torch.float32, (1,)), sf_layout=B.NVFP4_SF_TILED_ROWS)
     B.nvfp4_linear(xq, xs, gs.view(torch.float32, (1,)).clone(), M, wq["w1_codes"][0],
                    wq["w1_sf"][: B.nvfp4_sf_bytes(N, K)], wq["gs_w1"][:1],
                    out=lin.view(torch.bfloat16, (M, N + 8))[:, :N], ws=lws.bytes())
@@ -168,7 +169,7 @@ def test_route_and_quantize_dispatch_write_only_their_outputs():
     offsets, p2f, f2p = B.moe_permute(ids.view(torch.int32, (T, k)), E)
     a_rows = B.nvfp4moe_padded_rows(T * k, E)
     codes = Guarded(a_rows * K // 2)
-    sf = Guarded(B.nvfp4_sf_bytes(a_rows, K))
+    sf = Guarded(B.nvfp4_sf_bytes(a_rows, K, B.NVFP4_SF_TILED_ROWS))
     gs = Guarded(4)
     ws = Guarded(int(L.moe_quantize_dispatch_workspace_size(E)))
     inputs = {"x": x, "offsets": offsets, "f2p": f2p}

@@ -220,11 +220,10 @@ extern "C" int moe_dispatch_static(const void* x, int64_t ldx, const float* rout
 
 extern "C" int moe_dispatch_supported(int64_t T, int E, int k) { return moe_front_fits(T, E, k) ? 1 : 0; }
 
-// Measured on GB300: the fused dispatch saves the separate launches below
-// ~65536 routed rows (decode: 21 us against 38 us), matches them at 65536
-// (0.164 vs 0.168 ms), and is slower above (131072 rows: 0.36 vs 0.30 ms),
-// where the separate kernels' full-occupancy grids stream x faster than its
-// co-resident blocks.
+// Measured on GB300: the fused dispatch saves the separate launches up to
+// 65536 routed rows (decode: 21 us against 38 us; 65536 rows: 0.144 ms) and
+// is slower above (131072 rows: 0.28 against 0.25 ms), where the separate
+// kernels' full-occupancy grids stream x faster than its co-resident blocks.
 extern "C" int moe_forward_uses_fused_dispatch(int64_t T, int E, int k) {
   return T >= 1 && T * k <= 65536 && moe_front_fits(T, E, k) ? 1 : 0;
 }

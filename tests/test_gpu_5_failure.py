@@ -51,8 +51,10 @@ def test_wait_timeout_is_reported_and_context_survives():
     assert torch.isfinite(good.float()).all()
 
 
-def test_front_barrier_timeout_is_reported_and_context_survives():
-    """moe_forward_static: with the test stall on, block 0 of the fused front
+@pytest.mark.parametrize("front", ["static", "dynamic"])
+def test_front_barrier_timeout_is_reported_and_context_survives(front):
+    """The fused front (moe_forward_static with its given global scale, or
+    moe_forward, whose dispatch computes it): with the test stall on, block 0
     leaves before the first grid barrier; the other blocks' bounded barrier
     waits run out, the status reads NVFP4MOE_ERR_DEVICE_TIMEOUT, the later
     stages find no rows, and the next normal call gives the normal result."""
@@ -62,17 +64,22 @@ def test_front_barrier_timeout_is_reported_and_context_survives():
     wts = B.prepare_moe_weights(inp["w1"], inp["w2"])
     gs_h = torch.tensor([cfg.gs_h], dtype=torch.float32, device=DEV)
     gs_x = torch.tensor([500.0], dtype=torch.float32, device=DEV)
-    good = B.moe_forward_static(inp["x"], inp["logits"], wts, cfg.k, gs_h, gs_x).clone()
+    if front == "static":
+        fwd = lambda: B.moe_forward_static(inp["x"], inp["logits"], wts, cfg.k, gs_h, gs_x)
+    else:
+        assert B.moe_forward_uses_fused_dispatch(cfg.T, cfg.E, cfg.k)
+        fwd = lambda: B.moe_forward(inp["x"], inp["logits"], wts, cfg.k, gs_h)
+    good = fwd().clone()
     assert B.nvfp4moe_last_device_status() == 0
     try:
         B.nvfp4moe_set_wait_limit_ns(20_000_000)
         B.nvfp4moe_set_test_stall(True)
-        B.moe_forward_static(inp["x"], inp["logits"], wts, cfg.k, gs_h, gs_x)
+        fwd()
         st = B.nvfp4moe_last_device_status()
     finally:
         B.nvfp4moe_set_test_stall(False)
         B.nvfp4moe_set_wait_limit_ns(4_000_000_000)
     assert st == -5
-    again = B.moe_forward_static(inp["x"], inp["logits"], wts, cfg.k, gs_h, gs_x)
+    again = fwd()
     assert B.nvfp4moe_last_device_status() == 0
     assert torch.equal(good, again)

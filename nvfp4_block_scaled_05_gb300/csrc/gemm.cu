@@ -18,19 +18,23 @@
 //   warp 0      TMA producer: A and B code tiles (tiled TMA, 128B swizzle)
 //               into a 4-stage ring
 //   warp 1      TMEM owner; one lane issues the MMAs
-//   warps 2-5   scale warps, one per TMEM lane quadrant q. The scale atoms
-//               reach a shared-memory ring either by the producer's bulk
-//               copies (L1) or by the scale warps' own cp.async copies up to 4
-//               stages ahead (L2: the load path adds to the TMA engine's
-//               bandwidth, which the code tiles saturate). Per K=64 step the A
-//               scale of each of the quadrant's 32 rows goes to column 4kk+q
-//               (the MMA reads quadrant q's A scales from column base+q), and
-//               the 256 B-row scales to columns 8kk..8kk+7 (B scales are read
-//               in every quadrant, so each quadrant holds its own copy)
+//   warps 2-5   scale warps, one per TMEM lane quadrant q. A stage's scales
+//               (activation: 128 rows x 16 bytes, row-tiled layout; weights:
+//               512-byte atoms) reach a shared-memory ring either by the
+//               producer's bulk copies (L1) or by the scale warps' own
+//               cp.async copies up to 4 stages ahead (L2: the load path adds
+//               to the TMA engine's bandwidth, which the code tiles
+//               saturate). Per K=64 step the A scale of each of the quadrant's
+//               32 rows goes to column 4kk+q (the MMA reads quadrant q's A
+//               scales from column base+q), and the 256 B-row scales to
+//               columns 8kk..8kk+7 (B scales are read in every quadrant, so
+//               each quadrant holds its own copy)
 //   warps 6-13  epilogue, two warps per TMEM lane quadrant (128 columns
 //               each): the f32 accumulator is moved to registers and released
-//               at once, so the next tile's MMAs overlap the epilogue math;
-//               then BF16 output (L2) or SwiGLU + NVFP4 requant (L1)
+//               (L1: the first 64 columns become h before the second 64 are
+//               loaded), so the next tile's MMAs overlap the epilogue math;
+//               then BF16 output (L2, streaming stores) or SwiGLU + NVFP4
+//               requant (L1, h in the row-tiled scale layout the L2 GEMM reads)
 // Tiles are ordered expert-major, then weight tile, then activation tile, so
 // the activation tiles sharing one weight tile run at the same time on
 // neighbouring SMs and the weight tile leaves HBM once.

@@ -108,3 +108,18 @@ def test_global_scale():
     assert O.global_scale(6.0) == np.float32(448.0)
     a = np.float32(5.123)
     assert O.global_scale(a) == np.float32(2688.0) / a
+
+
+def test_amax_is_the_largest_magnitude():
+    """amax = max |x| (the activation global scale is 2688 / amax): the extreme
+    element may be negative."""
+    rng = np.random.default_rng(11)
+    x = rng.normal(0, 1, (6, 48)).astype(np.float32)
+    x[4, 17] = -9.5
+    xb = torch.from_numpy(x).to(torch.bfloat16)
+    bits = xb.view(torch.int16).numpy().view(np.uint16)
+    ref = float(xb.float().abs().max())
+    assert ref == 9.5
+    assert O.amax_bf16(bits) == np.float32(ref)
+    assert O.amax_f32(x) == np.float32(np.abs(x).max())
+    assert O.global_scale(O.amax_bf16(bits)) == np.float32(2688.0) / np.float32(9.5)

@@ -174,6 +174,39 @@ def test_moe_forward_single_expert_is_a_two_layer_mlp():
     assert np.allclose(r["y"], y, rtol=1e-12, atol=1e-14)
 
 
+def test_moe_forward_is_the_routing_weighted_sum_of_expert_mlps():
+    """E=3, k=2: y[t] = sum_j w[t, j] * MLP_{ids[t, j]}(x[t]), with the top-2 and
+    its softmax from torch and each expert's two-layer MLP composed in numpy on
+    dequantized operands."""
+    rng = np.random.default_rng(8)
+    T, K, I, E, k = 6, 64, 32, 3, 2
+    x = bf16_bits_np(rng.normal(0, 1, (T, K)))
+    w1 = [bf16_bits_np(rng.normal(0, 0.1, (2 * I, K))) for _ in range(E)]
+    w2 = [bf16_bits_np(rng.normal(0, 0.1, (K, I))) for _ in range(E)]
+    logits = rng.normal(0, 1, (T, E)).astype(np.float32)
+    gs_h = np.float32(400.0)
+    r = O.moe_forward(x, logits, lambda e: w1[e], lambda e: w2[e], k, gs_h)
+    top = torch.topk(torch.from_numpy(logits).double(), k, dim=1)
+    ids = top.indices.numpy()
+    wts = torch.softmax(top.values, dim=1).numpy()
+    gx = O.global_scale(O.amax_bf16(x))
+    xd = O.dequantize_f64(*O.quantize_bf16(x, gx), gx)
+
+    def mlp(e, xrow):
+        c1, s1, g1 = O.quantize_expert(w1[e])
+        c2, s2, g2 = O.quantize_expert(w2[e])
+        v = xrow[None, :] @ O.dequantize_f64(c1, s1, g1).T
+        g, u = v[:, :I], v[:, I:]
+        h = (g / (1 + np.exp(-g)) * u).astype(np.float32)
+        hd = O.dequantize_f64(*O.quantize_f32(h, gs_h), gs_h)
+        return (hd @ O.dequantize_f64(c2, s2, g2).T)[0]
+
+    assert len({tuple(sorted(r)) for r in ids}) > 1       # more than one expert pair in use
+    for t in range(T):
+        y = sum(wts[t, j] * mlp(int(ids[t, j]), xd[t]) for j in range(k))
+        assert np.allclose(r["y"][t], y, rtol=1e-12, atol=1e-14), t
+
+
 def bf16_bits_np(a):
     return W.bf16_bits(torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16))
 

@@ -51,6 +51,12 @@ def test_underflow_threshold_in_scaled_domain():
         v[0, 0] = amax
         codes, sf = O.quantize_f32(v, gs)
         assert (sf[0, 0] == 0 and not codes.any()) == expect_zero, amax
+    # exactly at the threshold the block is not an underflow block (the rule is
+    # amax < 6*2^-9, strict): scale 2^-9 (E4M3 code 1) and the element maps to 6
+    v = np.zeros((1, 16), np.float32)
+    v[0, 3] = np.float32(thr / 4)
+    codes, sf = O.quantize_f32(v, np.float32(4.0))
+    assert sf[0, 0] == 1 and codes[0, 1] == 0x70 and codes.sum() == 0x70
     # a raw block maximum below 6*2^-9 is still a normal block when gs is large
     v = np.full((1, 16), 0.005, np.float32)
     codes, sf = O.quantize_f32(v, np.float32(100.0))
@@ -132,6 +138,7 @@ def test_interleave_identity_and_granularity():
     assert np.array_equal(il[16:24], a[8:16])
     assert np.array_equal(il[24:32], a[I + 8:I + 16])
     assert not np.array_equal(il, O.interleave_rows(a, 4))
+    assert np.array_equal(O.interleave_rows(a), il) and np.array_equal(O.deinterleave_rows(il), a)
 
 
 def test_interleave_commutes_with_quantize():

@@ -54,6 +54,13 @@ def test_quantize_rowmajor_and_ragged_cols():
     _quant_check(torch.randn(129, 592, generator=g).to(torch.bfloat16))
 
 
+def test_quantize_global_scale_from_a_negative_extreme():
+    g = torch.Generator().manual_seed(15)
+    x = torch.randn(40, 256, generator=g)
+    x[17, 100] = -23.5
+    _quant_check(x.to(torch.bfloat16))
+
+
 def test_quantize_precomputed_gs():
     g = torch.Generator().manual_seed(13)
     _quant_check((torch.randn(64, 512, generator=g) * 3).to(torch.bfloat16), gs_given=17.25)
@@ -146,3 +153,24 @@ def test_dispatch_quantize_padded_rows_bit_exact():
         t = p2f[r] // cfg.k
         assert np.array_equal(gc[prow[r]], rc[t])
         assert np.array_equal(gsf[prow[r]], rs[t])
+
+
+def test_quantize_underflow_boundary():
+    """Blocks whose scaled maximum p = amax * gs sits exactly at 6 * 2^-9 (not an
+    underflow block: the rule is strict), one BF16 step below it (underflow:
+    scale 0, codes 0) and one step above."""
+    thr_raw = 3.0 * 2.0 ** -10                    # * gs 4 = 6 * 2^-9, exact in BF16
+    step = 2.0 ** -7 * 2.0 ** -9                  # one BF16 ulp at 1.5 * 2^-9
+    rows = []
+    for amax in (thr_raw, thr_raw - step, thr_raw + step):
+        for sign in (1.0, -1.0):
+            r = np.zeros(64, np.float32)
+            r[5] = sign * amax
+            r[9] = amax / 4
+            r[16 + 2] = sign * amax                   # a second block in the row
+            rows.append(r)
+    x = torch.from_numpy(np.stack(rows)).to(torch.bfloat16)
+    _, sf = _quant_check(x, gs_given=4.0, layout=B.NVFP4_SF_ROWMAJOR)
+    assert np.all(sf[0:2, 0:2] == 1)                  # exactly at the threshold: 2^-9
+    assert np.all(sf[2:4, 0:2] == 0)                  # below: underflow
+    assert np.all(sf[4:6, 0:2] != 0)

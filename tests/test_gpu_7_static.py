@@ -214,14 +214,16 @@ def test_fused_dispatch_equals_separate_calls(name):
 
 def test_fused_dispatch_edge_shapes():
     """T=1; more experts than routed rows (E=1000); every token on one expert;
-    an all-zero x (global scale 1)."""
+    an all-zero x (global scale 1); the largest |x| a negative element."""
     for (T, K, E, k, mode) in [(1, 256, 8, 2, "rand"), (3, 384, 1000, 4, "rand"), (200, 256, 4, 1, "one"),
-                               (64, 512, 16, 2, "zero")]:
+                               (64, 512, 16, 2, "zero"), (96, 256, 8, 2, "negmax")]:
         cfg = W.MoEConfig("edge", T=T, K=K, I=64, E=E, k=k, gs_h=336.0)
         g = torch.Generator(device="cpu").manual_seed(T + E)
         x = torch.randn(T, K, generator=g).to(torch.bfloat16)
         if mode == "zero":
             x.zero_()
+        if mode == "negmax":
+            x[T // 2, K - 3] = -40.0
         logits = torch.randn(T, E, generator=g)
         if mode == "one":
             logits[:, 2] += 100.0
@@ -229,5 +231,7 @@ def test_fused_dispatch_edge_shapes():
         assert fused["gs_x"] == split["gs_x"], (T, E)
         if mode == "zero":
             assert fused["gs_x"] == 1.0
+        if mode == "negmax":
+            assert fused["gs_x"] == O.global_scale(O.amax_bf16(W.bf16_bits(x))) == np.float32(2688.0 / 40.0)
         for n in NAMES + ["rows", "sf"]:
             assert np.array_equal(fused[n], split[n]), (n, T, E)

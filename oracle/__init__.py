@@ -328,11 +328,9 @@ def moe_forward(x, logits, get_w1, get_w2, k, gs_h, tokens=None, keep=False, exp
             outs[ti, j] = o[r]
             if keep:
                 inter[(tokens[ti], j)] = dict(v=v[r], h=h[r], hc=hc[r], hs=hs[r], o=o[r])
-    # step 6: weighted sum over j, in j order, fp64
-    y = np.zeros((len(tokens), K), np.float64)
-    wt = w[tokens]
-    for j in range(k):
-        y += wt[:, j:j + 1] * outs[:, j]
+    # step 6: weighted sum over j, in j order, fp64 (slot (ti, j) is row ti*k + j of outs)
+    n = len(tokens)
+    y = combine(outs.reshape(n * k, K), w[tokens], np.arange(n * k, dtype=np.int32))
     return dict(ids=ids, w=w, offsets=offsets, perm_to_flat=p2f, flat_to_perm=f2p,
                 amax_x=amax_x, gs_x=gs_x, tokens=tokens, x_codes=xc, x_sf=xs, y=y,
                 inter=inter, gs_w=gs_w)

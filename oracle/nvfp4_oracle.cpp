@@ -35,6 +35,8 @@
 //      every step one f32 operation rounded to nearest.
 //   R5 top-k: the k largest logits, ties to the lower expert index, ordered by
 //      descending logit; weights = softmax over the k selected logits.
+//   R16 a NaN router logit ranks as -inf: below every finite logit, never
+//      chosen before one, and never leaves a token without k experts.
 //   R6 permutation: rows of one expert are ordered by ascending flat slot
 //      f = t*k + j (stable counting sort).
 //   R7 dequantized value = code * s / gs; GEMMs accumulate in fp64.
@@ -287,19 +289,23 @@ void orc_deinterleave_rows(const uint8_t* src, uint8_t* dst, int64_t two_i, int6
 
 // ---------------------------------------------------------------- routing
 
-// R5 for T tokens over E experts.
+// R5 for T tokens over E experts. R16: a NaN logit ranks as -inf (below every
+// finite logit, tied with -inf, ties to the lower index), so the sort key is a
+// strict weak order and a token with NaN logits still gets k valid experts.
 void orc_route_topk(const float* logits, int64_t T, int E, int k, int32_t* ids, double* w) {
   std::vector<int> idx(E);
+  std::vector<double> key(E);
   for (int64_t t = 0; t < T; ++t) {
     const float* l = logits + t * E;
+    for (int e = 0; e < E; ++e) key[e] = std::isnan(l[e]) ? -INFINITY : (double)l[e];
     std::iota(idx.begin(), idx.end(), 0);
-    std::stable_sort(idx.begin(), idx.end(), [&](int a, int b) { return l[a] > l[b]; });
-    double lmax = l[idx[0]];
+    std::stable_sort(idx.begin(), idx.end(), [&](int a, int b) { return key[a] > key[b]; });
+    double lmax = key[idx[0]];
     double den = 0.0;
-    for (int j = 0; j < k; ++j) den += std::exp((double)l[idx[j]] - lmax);
+    for (int j = 0; j < k; ++j) den += std::exp(key[idx[j]] - lmax);
     for (int j = 0; j < k; ++j) {
       ids[t * k + j] = idx[j];
-      w[t * k + j] = std::exp((double)l[idx[j]] - lmax) / den;
+      w[t * k + j] = std::exp(key[idx[j]] - lmax) / den;
     }
   }
 }

@@ -33,6 +33,27 @@ def test_route_ties_and_odd_expert_counts():
         assert np.allclose(w.cpu().numpy(), rw, rtol=1e-6, atol=1e-7)
 
 
+def test_route_nan_logits_decode_shape():
+    """Reading R16 (a NaN logit ranks as -inf) on a decode-shaped batch (T=128,
+    E=256, top-8) with NaN logits scattered over it, including rows whose
+    largest logit position holds a NaN and a row with fewer than k finite
+    logits: ids bit-exact against the oracle, weights within 1e-6."""
+    rng = np.random.default_rng(11)
+    T, E, k = 128, 256, 8
+    logits = rng.normal(0, 1, (T, E)).astype(np.float32)
+    logits[rng.random((T, E)) < 0.05] = np.nan
+    top = np.argmax(np.nan_to_num(logits, nan=-np.inf), axis=1)
+    logits[np.arange(0, T, 3), top[::3]] = np.nan          # the would-be winner is NaN
+    logits[5, :] = np.nan
+    logits[5, [17, 200, 3, 99, 64]] = [0.5, -1.0, 2.0, 0.0, 1.5]   # 5 finite logits, k = 8
+    ids, w = B.moe_route_topk(torch.from_numpy(logits).to(DEV), k)
+    torch.cuda.synchronize()
+    rid, rw = O.route_topk(logits, k)
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    assert np.allclose(w.cpu().numpy(), rw, rtol=1e-6, atol=1e-7)
+    assert np.all(np.isfinite(w.cpu().numpy()))
+
+
 @pytest.mark.parametrize("T,k,E,mode", [(1, 1, 1, "uniform"), (64, 2, 8, "uniform"),
                                          (128, 8, 256, "uniform"), (16384, 8, 256, "uniform"),
                                          (5000, 8, 256, "one"), (3000, 4, 1000, "sparse"),

@@ -235,3 +235,23 @@ def test_fused_dispatch_edge_shapes():
             assert fused["gs_x"] == O.global_scale(O.amax_bf16(W.bf16_bits(x))) == np.float32(2688.0 / 40.0)
         for n in NAMES + ["rows", "sf"]:
             assert np.array_equal(fused[n], split[n]), (n, T, E)
+
+
+def test_fused_dispatch_nan_logits():
+    """Reading R16 in the fused dispatch: NaN router logits scattered over a
+    decode-shaped batch rank as -inf. Routing equals the oracle's (ids bit for
+    bit, weights within 1e-6) and every intermediate equals the separate
+    calls' bit for bit."""
+    cfg = W.CONFIGS["decode"]
+    inp = W.moe_inputs(cfg, seed=9, device="cpu", weights=False)
+    logits = inp["logits"].numpy().copy()
+    rng = np.random.default_rng(12)
+    logits[rng.random(logits.shape) < 0.05] = np.nan
+    rows = np.arange(0, logits.shape[0], 4)
+    logits[rows, np.argmax(np.nan_to_num(logits[rows], nan=-np.inf), axis=1)] = np.nan
+    split, fused = _split_and_fused(cfg, inp["x"].to(DEV), torch.from_numpy(logits).to(DEV))
+    rid, rw = O.route_topk(logits, cfg.k)
+    assert np.array_equal(fused["topk_ids"].reshape(rid.shape), rid)
+    assert np.allclose(fused["topk_w"].reshape(rw.shape), rw, rtol=1e-6, atol=1e-7)
+    for n in NAMES + ["rows", "sf"]:
+        assert np.array_equal(fused[n], split[n]), n

@@ -39,6 +39,31 @@ def test_route_ignores_minus_inf_experts():
     assert np.allclose(w, 1 / 6)
 
 
+def test_route_nan_logits_rank_as_minus_inf():
+    """Reading R16: a NaN logit ranks as -inf (ties with -inf to the lower
+    index); checked against numpy's stable argsort of the logits with NaN
+    replaced by -inf, and torch's softmax over the selected values."""
+    rng = np.random.default_rng(7)
+    T, E, k = 300, 64, 8
+    logits = rng.normal(0, 1, (T, E)).astype(np.float32)
+    logits[rng.random((T, E)) < 0.1] = np.nan      # scattered NaNs
+    logits[:20, 0] = np.nan                        # a NaN in front of every other logit
+    logits[20, :] = np.nan                         # a NaN-only row except three finite logits
+    logits[20, [5, 40, 63]] = [1.0, -2.0, 3.0]
+    logits[21, :] = -np.inf                        # NaN and -inf tie: lower index first
+    logits[21, [2, 9]] = np.nan
+    logits[21, 30] = 0.0
+    ids, w = O.route_topk(logits, k)
+    mapped = np.where(np.isnan(logits), -np.inf, logits)
+    ref = np.argsort(-mapped, axis=1, kind="stable")[:, :k]
+    assert np.array_equal(ids, ref)
+    assert list(ids[20, :3]) == [63, 5, 40] and list(ids[21, :3]) == [30, 0, 1]
+    sel = np.take_along_axis(mapped, ref, axis=1)
+    ref_w = torch.softmax(torch.from_numpy(sel).double(), dim=1).numpy()
+    assert np.allclose(w, ref_w, rtol=0, atol=1e-14)
+    assert np.all(w[20, 3:] == 0.0) and np.all(np.isfinite(w))
+
+
 def test_permute_vs_stable_argsort_and_bincount():
     rng = np.random.default_rng(1)
     for T, k, E in [(1, 1, 1), (50, 2, 8), (300, 8, 64), (64, 4, 300)]:

@@ -75,8 +75,10 @@ MUTANTS = [
     # routing and permutation
     ("softmax_over_all_experts", CPP, "for (int j = 0; j < k; ++j) den += std::exp",
      "for (int j = 0; j < E; ++j) den += std::exp"),
-    ("topk_ties_to_higher_index", CPP, "std::stable_sort(idx.begin(), idx.end(), [&](int a, int b) { return l[a] > l[b]; });",
-     "std::stable_sort(idx.begin(), idx.end(), [&](int a, int b) { return l[a] > l[b] || (l[a] == l[b] && a > b); });"),
+    ("topk_ties_to_higher_index", CPP, "std::stable_sort(idx.begin(), idx.end(), [&](int a, int b) { return key[a] > key[b]; });",
+     "std::stable_sort(idx.begin(), idx.end(), [&](int a, int b) { return key[a] > key[b] || (key[a] == key[b] && a > b); });"),
+    ("topk_nan_not_ranked_as_minus_inf", CPP,
+     "key[e] = std::isnan(l[e]) ? -INFINITY : (double)l[e];", "key[e] = (double)l[e];"),
     ("permutation_not_stable", CPP,
      "  for (int64_t f = 0; f < T * k; ++f) {\n    int64_t pos = next[ids[f]]++;",
      "  for (int64_t f = T * k - 1; f >= 0; --f) {\n    int64_t pos = next[ids[f]]++;"),
@@ -105,7 +107,8 @@ MUTANTS = [
     # the forward's composition (oracle/__init__.py)
     ("forward_h_dequantized_with_gs_x", PY, "o = matmul_nt(dequantize_f64(hc, hs, gs_h)",
      "o = matmul_nt(dequantize_f64(hc, hs, gs_x)"),
-    ("forward_unweighted_sum", PY, "y += wt[:, j:j + 1] * outs[:, j]", "y += outs[:, j]"),
+    ("forward_unweighted_sum", PY, "y = combine(outs.reshape(n * k, K), w[tokens],",
+     "y = combine(outs.reshape(n * k, K), np.ones_like(w[tokens]),"),
     ("forward_w1_with_w2_scale", PY, "v = matmul_nt(a, dequantize_f64(c1, s1, g1))",
      "v = matmul_nt(a, dequantize_f64(c1, s1, g2))"),
     ("forward_gs_x_ignored_when_given", PY,

@@ -117,6 +117,48 @@ int64_t nvfp4moe_padded_rows(int64_t M, int E);
  * Returns NVFP4MOE_OK or NVFP4MOE_ERR_INVALID. */
 int nvfp4moe_interleave_row_map(int64_t two_i, int32_t* map_host);
 
+/*
+ * Offline layout helpers (README "Bridge Layer": assemble_scales_2d_side /
+ * assemble_scales_3d_side assemble scale factors into the layout the MMA
+ * reads; interleave_l1_weights / deinterleave_l1_weights). Untimed weight
+ * preparation; each launches one gather kernel on `stream` and allocates
+ * nothing. Inputs and outputs must not overlap.
+ *
+ * nvfp4_sf_to_tiled -- `batch` scale matrices of (rows x cols) elements, each
+ * rows x cols/16 row-major bytes (matrix m at byte m * rows * cols/16), into
+ * the tiled layout sf_layout (NVFP4_SF_TILED or NVFP4_SF_TILED_ROWS), matrix m
+ * at byte m * nvfp4_sf_bytes(rows, cols, sf_layout). Every byte of the tiled
+ * output is written; padding rows and columns get 0. For the expert weights
+ * of the grouped GEMMs: batch = E, (rows, cols) = (N, K), NVFP4_SF_TILED.
+ * nvfp4_sf_from_tiled -- the inverse: the rows x cols/16 valid bytes of each
+ * tiled matrix, row-major.
+ * Errors: INVALID (cols % 16 != 0, negative sizes, null pointer, bad layout),
+ * LAUNCH.
+ */
+int nvfp4_sf_to_tiled(const uint8_t* sf, int64_t batch, int64_t rows, int64_t cols, int sf_layout,
+                      uint8_t* sf_tiled, void* stream);
+int nvfp4_sf_from_tiled(const uint8_t* sf_tiled, int64_t batch, int64_t rows, int64_t cols, int sf_layout,
+                        uint8_t* sf, void* stream);
+
+/*
+ * nvfp4_interleave_gate_up -- README "Fused SwiGLU - How It Works": W1's 2I
+ * rows [gate 0..I-1 | up 0..I-1] reordered so that rows are interleaved at
+ * granularity 8 ([g0-7, u0-7, g8-15, u8-15, ...]: row 16*(i/8) + i%8 is gate
+ * row i and row 16*(i/8) + 8 + i%8 is up row i), or back (inverse = 1). Whole
+ * NVFP4 rows move, since the 16-element blocks run along K.
+ *   codes / codes_out  batch x two_i x K/2 bytes (NULL both to skip).
+ *   sf / sf_out        batch scale matrices of (two_i, K) in sf_layout
+ *                      (NVFP4_SF_ROWMAJOR, NVFP4_SF_TILED or
+ *                      NVFP4_SF_TILED_ROWS), matrix m at byte
+ *                      m * nvfp4_sf_bytes(two_i, K, sf_layout); the same
+ *                      layout in and out, tiled padding written 0 (NULL both
+ *                      to skip).
+ * Requires two_i % 16 == 0, K % 16 == 0, batch <= 65535. Errors: INVALID,
+ * UNSUPPORTED, LAUNCH.
+ */
+int nvfp4_interleave_gate_up(const uint8_t* codes, const uint8_t* sf, int64_t batch, int64_t two_i, int64_t K,
+                             int sf_layout, int inverse, uint8_t* codes_out, uint8_t* sf_out, void* stream);
+
 /* Workspace bytes nvfp4_quantize needs when it computes the global scale. */
 size_t nvfp4_quantize_workspace_size(void);
 

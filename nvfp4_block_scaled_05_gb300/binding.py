@@ -27,6 +27,10 @@ _SIGS = {
     "nvfp4_sf_bytes": (_size, [_i64, _i64, _int]),
     "nvfp4moe_padded_rows": (_i64, [_i64, _int]),
     "nvfp4moe_interleave_row_map": (_int, [_i64, _c_void_p]),
+    "nvfp4_sf_to_tiled": (_int, [_c_void_p, _i64, _i64, _i64, _int, _c_void_p, _c_void_p]),
+    "nvfp4_sf_from_tiled": (_int, [_c_void_p, _i64, _i64, _i64, _int, _c_void_p, _c_void_p]),
+    "nvfp4_interleave_gate_up": (_int, [_c_void_p, _c_void_p, _i64, _i64, _i64, _int, _int, _c_void_p,
+                                        _c_void_p, _c_void_p]),
     "nvfp4_quantize_workspace_size": (_size, []),
     "nvfp4_quantize": (_int, [_c_void_p, _i64, _i64, _i64, _c_void_p, _c_void_p, _c_void_p,
                               _c_void_p, _c_void_p, _int, _c_void_p, _size, _c_void_p]),
@@ -134,6 +138,48 @@ def nvfp4moe_interleave_row_map(two_i):
     m = (ctypes.c_int32 * two_i)()
     _check(lib().nvfp4moe_interleave_row_map(two_i, ctypes.cast(m, ctypes.c_void_p)), "interleave_row_map")
     return torch.tensor(list(m), dtype=torch.int32)
+
+
+def nvfp4_sf_to_tiled(sf, rows, cols, sf_layout=NVFP4_SF_TILED, out=None):
+    """Row-major scales (batch, rows, cols//16) or (rows, cols//16) -> the tiled
+    layout, batch * nvfp4_sf_bytes(rows, cols, sf_layout) bytes (README "Bridge
+    Layer": assemble_scales_2d_side / _3d_side)."""
+    _dev(sf, "sf")
+    batch = sf.numel() // max(1, rows * (cols // 16))
+    per = nvfp4_sf_bytes(rows, cols, sf_layout)
+    if out is None:
+        out = torch.empty(batch * per, dtype=torch.uint8, device=sf.device)
+    _check(lib().nvfp4_sf_to_tiled(_ptr(sf), batch, rows, cols, sf_layout, _ptr(out), _stream()),
+           "nvfp4_sf_to_tiled")
+    return out
+
+
+def nvfp4_sf_from_tiled(sf_tiled, batch, rows, cols, sf_layout=NVFP4_SF_TILED, out=None):
+    """Tiled scales of `batch` (rows x cols) matrices -> (batch, rows, cols//16) row-major."""
+    _dev(sf_tiled, "sf_tiled")
+    if out is None:
+        out = torch.empty((batch, rows, cols // 16), dtype=torch.uint8, device=sf_tiled.device)
+    _check(lib().nvfp4_sf_from_tiled(_ptr(sf_tiled), batch, rows, cols, sf_layout, _ptr(out), _stream()),
+           "nvfp4_sf_from_tiled")
+    return out
+
+
+def nvfp4_interleave_gate_up(codes, sf, two_i, K, sf_layout=NVFP4_SF_ROWMAJOR, inverse=False):
+    """W1 rows [gate | up] <-> interleaved at granularity 8 (README "Bridge
+    Layer": interleave_l1_weights / deinterleave_l1_weights). codes: (batch,
+    two_i, K//2) bytes or None; sf: batch scale matrices in sf_layout or None.
+    Returns (codes_out, sf_out)."""
+    if codes is not None:
+        _dev(codes, "codes")
+    if sf is not None:
+        _dev(sf, "sf")
+    batch = (codes.numel() // (two_i * (K // 2))) if codes is not None else \
+        (sf.numel() // nvfp4_sf_bytes(two_i, K, sf_layout))
+    co = torch.empty_like(codes) if codes is not None else None
+    so = torch.empty_like(sf) if sf is not None else None
+    _check(lib().nvfp4_interleave_gate_up(_ptr(codes), _ptr(sf), batch, two_i, K, sf_layout, int(bool(inverse)),
+                                          _ptr(co), _ptr(so), _stream()), "nvfp4_interleave_gate_up")
+    return co, so
 
 
 def nvfp4moe_num_sms():

@@ -14,7 +14,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libnvfp4moe.so")
-SOURCES = ["quantize.cu", "routing.cu", "front.cu", "gemm.cu", "api.cu"]
+SOURCES = ["quantize.cu", "routing.cu", "front.cu", "gemm.cu", "api.cu", "layout.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 

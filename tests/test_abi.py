@@ -132,3 +132,20 @@ def test_host_fault_injection_rejected_before_any_launch(lib):
     lib.moe_permute_workspace_size.restype = ctypes.c_size_t
     pws = lib.moe_permute_workspace_size(i64(T), k, E)
     assert lib.moe_permute(p, i64(T), k, E, p, p, p, p, sz(pws - 1), None) == -3
+
+
+def test_layout_helpers_reject_bad_arguments(lib):
+    """The offline layout helpers check their arguments on the host."""
+    vp, i64 = ctypes.c_void_p, ctypes.c_int64
+    for name in ["nvfp4_sf_to_tiled", "nvfp4_sf_from_tiled", "nvfp4_interleave_gate_up"]:
+        getattr(lib, name).restype = ctypes.c_int
+    p, q = vp(1 << 20), vp(1 << 21)
+    assert lib.nvfp4_sf_to_tiled(p, i64(1), i64(128), i64(40), 1, q, None) == -1     # cols % 16
+    assert lib.nvfp4_sf_to_tiled(p, i64(1), i64(128), i64(64), 0, q, None) == -1     # row-major is not tiled
+    assert lib.nvfp4_sf_from_tiled(None, i64(1), i64(128), i64(64), 2, q, None) == -1
+    assert lib.nvfp4_sf_to_tiled(None, i64(0), i64(128), i64(64), 1, None, None) == 0  # nothing to do
+    assert lib.nvfp4_interleave_gate_up(p, None, i64(1), i64(24), i64(64), 0, 0, q, None, None) == -1  # 2I % 16
+    assert lib.nvfp4_interleave_gate_up(p, None, i64(1), i64(32), i64(64), 0, 2, q, None, None) == -1  # inverse
+    assert lib.nvfp4_interleave_gate_up(p, None, i64(1), i64(32), i64(64), 0, 0, None, None, None) == -1
+    assert lib.nvfp4_interleave_gate_up(p, None, i64(1), i64(32), i64(64), 0, 0, p, None, None) == -1  # in place
+    assert lib.nvfp4_interleave_gate_up(p, p, i64(1), i64(32), i64(64), 3, 0, q, q, None) == -1      # layout

@@ -48,7 +48,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="prefill",
-                    choices=["tiny", "decode", "prefill", "skewed", "prefill_small", "decode_small", "prefill_med",
+                    choices=["tiny", "decode", "prefill", "skewed", "prefill_small", "decode_small", "prefill_med", "skewed_small",
                              "dsv4_decode", "dsv4_prefill"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
@@ -205,7 +205,11 @@ def ncu_traffic(workload):
 
 
 def layer_numbers(cfg, offsets):
-    """Algorithmic FLOPs and bytes of one forward and of the L1 kernel."""
+    """Algorithmic FLOPs and bytes of one forward and of the L1 kernel.
+
+    The L1 kernel's algorithmic bytes are its active experts' W1 codes and
+    scales only; the activation rows it reads (A) and the h rows it writes are
+    pipeline bytes between kernels, reported apart (l1_pipeline_bytes)."""
     counts = [offsets[e + 1] - offsets[e] for e in range(cfg.E)]
     active = sum(1 for c in counts if c > 0)
     K, I, M, T = cfg.K, cfg.I, cfg.M, cfg.T
@@ -214,8 +218,25 @@ def layer_numbers(cfg, offsets):
     flops = 6.0 * M * K * I
     layer_bytes = active * (w1 + w2) + T * K * 2 * 2 + T * cfg.E * 4
     l1_flops = 4.0 * M * K * I
-    l1_bytes = active * w1 + M * (K // 2 + K // 16) + M * (I // 2 + I // 16)
-    return dict(active=active, flops=flops, bytes=layer_bytes, l1_flops=l1_flops, l1_bytes=l1_bytes)
+    l1_bytes = active * w1
+    l1_pipeline = M * (K // 2 + K // 16) + M * (I // 2 + I // 16)
+    return dict(active=active, flops=flops, bytes=layer_bytes, l1_flops=l1_flops, l1_bytes=l1_bytes,
+                l1_pipeline_bytes=l1_pipeline)
+
+
+def l1_roofline(nums, l1_ms, hbm_peak, fp4_peak):
+    """Roofline of the L1 kernel: bound by W1 streaming (HBM) or by the FP4
+    tensor rate, whichever takes longer at the peaks; achieved = algorithmic
+    bytes (or FLOPs) over the kernel's measured time."""
+    t_hbm = nums["l1_bytes"] / (hbm_peak * 1e9)
+    t_tc = nums["l1_flops"] / (fp4_peak * 1e12)
+    if t_hbm >= t_tc:
+        achieved = nums["l1_bytes"] / (l1_ms * 1e-3) / 1e9
+        return {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                "frac": achieved / hbm_peak}
+    achieved = nums["l1_flops"] / (l1_ms * 1e-3) / 1e12
+    return {"bound": "tensor", "achieved": achieved, "peak": fp4_peak, "unit": "TFLOP/s",
+            "frac": achieved / fp4_peak}
 
 
 # ---------------------------------------------------------------- oracle legs
@@ -576,17 +597,12 @@ def run_ours(args, cfg):
     fp4_peak = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])) * FP4_OVER_BF16
     tflops, tokens_s = aggregate_throughput(nums["flops"], T, world, ms)
     # roofline of the dominant kernel (L1 grouped GEMM + SwiGLU + requant)
-    t_hbm = nums["l1_bytes"] / (hbm_peak * 1e9)
-    t_tc = nums["l1_flops"] / (fp4_peak * 1e12)
-    if t_hbm >= t_tc:
-        achieved = nums["l1_bytes"] / (l1_ms * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                "frac": achieved / hbm_peak}
-    else:
-        achieved = nums["l1_flops"] / (l1_ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": fp4_peak, "unit": "TFLOP/s",
-                "frac": achieved / fp4_peak}
+    roof = l1_roofline(nums, l1_ms, hbm_peak, fp4_peak)
+    roof["algorithmic"] = ("active experts x W1 codes and scales (%d x %d B)" %
+                           (nums["active"], 2 * I * (K // 2 + K // 16)) if roof["bound"] == "hbm" else
+                           "4*M*K*I FLOP")
     roof["traffic"] = ncu_traffic(cfg.name)
+    roof["l1_pipeline_bytes"] = nums["l1_pipeline_bytes"]
     roof["kernel"] = "l1_swiglu (grouped_gemm_kernel<true>)"
     roof["kernel_ms"] = l1_ms
     roof["peak_source"] = "%s (MEASURED_PEAKS.json)" % peak_kind if peak_kind == "measured" else "fallback"
@@ -628,6 +644,13 @@ def run_ours(args, cfg):
         "gpu_launches": kernels_per_step(T, k, fused_front) * args.steps,
         "clocks": clk,
     }
+    if world == 1 and cfg.name == "prefill" and not args.graph and not static:
+        # the other two layer targets (decode: HBM; skewed: FP4 tensor rate) on the same weights
+        line["also"] = measure_also(args, cfg, wts, dev, hbm_peak, fp4_peak)
+        line["gpu_launches_also"] = sum(kernels_per_step(W.CONFIGS[n].T, W.CONFIGS[n].k,
+                                                         B.moe_forward_uses_fused_dispatch(
+                                                             W.CONFIGS[n].T, W.CONFIGS[n].E, W.CONFIGS[n].k))
+                                        * v["steps"] for n, v in line["also"].items())
     if world == 1 and not args.no_cpu_baseline:
         M = cfg.M
         f2p_h = ws[lay["flat_to_perm"]:lay["flat_to_perm"] + 4 * M].view(torch.int32).cpu().numpy()
@@ -639,6 +662,73 @@ def run_ours(args, cfg):
     if pg is not None:
         pg.barrier()
         pg.destroy_process_group()
+
+
+def measure_also(args, base, wts, dev, hbm_peak, fp4_peak):
+    """The decode (T=128) and skewed (T=16384) workloads, measured in the same
+    run on the benchmarked layer's weights (all three workloads share K, I, E
+    and the weight seed, so the weights are the same tensors). Per workload:
+    ms per step over timed moe_forward calls (CUDA events, after warm-up; the
+    6.3 GB of weights streamed every step exceed L2), TFLOP/s, tokens/s,
+    % of HBM bandwidth and of the FP4 peak, and the L1 kernel's roofline
+    fraction from its own per-stage time."""
+    import torch
+    from nvfp4_block_scaled_05_gb300 import binding as B
+    from nvfp4_block_scaled_05_gb300 import workloads as W
+    out = {}
+    stream = torch.cuda.current_stream()
+    for name in ("decode", "skewed"):
+        cfg = W.CONFIGS[name]
+        if (cfg.K, cfg.I, cfg.E) != (base.K, base.I, base.E):
+            continue
+        inp = W.moe_inputs(cfg, seed=args.seed, device=dev, weights=False)
+        x, logits = inp["x"], inp["logits"]
+        T, K, I, E, k = cfg.T, cfg.K, cfg.I, cfg.E, cfg.k
+        ws = torch.empty(B.moe_forward_workspace_size(T, K, I, E, k), dtype=torch.uint8, device=dev)
+        y = torch.empty((T, K), dtype=torch.bfloat16, device=dev)
+        gs_h = torch.tensor([cfg.gs_h], dtype=torch.float32, device=dev)
+        steps = max(20, args.steps if name == "decode" else args.steps // 4)
+        for _ in range(max(3, args.warmup)):
+            B.moe_forward(x, logits, wts, k, gs_h, ws=ws, y=y)
+        torch.cuda.synchronize()
+        if B.nvfp4moe_last_device_status() != 0:
+            raise RuntimeError("device status after warm-up (%s)" % name)
+        clocks = ClockSampler(torch.cuda.current_device())
+        clocks.start()
+        time.sleep(0.6)
+        t0 = time.time()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            B.moe_forward(x, logits, wts, k, gs_h, ws=ws, y=y)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        clk = clocks.stop(t0, time.time())
+        ms = e0.elapsed_time(e1) / steps
+        names = B.forward_stages(T, E, k)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(steps)]
+        for i in range(steps):
+            B.moe_forward_stages(x, logits, wts, k, gs_h, ws, y, events=evs[i])
+        torch.cuda.synchronize()
+        if B.nvfp4moe_last_device_status() != 0:
+            raise RuntimeError("device status after timed region (%s)" % name)
+        stage_ms = {n: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps)) / steps
+                    for j, n in enumerate(names)}
+        lay = B.moe_forward_workspace_layout(T, K, I, E, k)
+        offsets = ws[lay["offsets"]:lay["offsets"] + 4 * (E + 1)].view(torch.int32).cpu().tolist()
+        nums = layer_numbers(cfg, offsets)
+        roof = l1_roofline(nums, stage_ms["l1_swiglu"], hbm_peak, fp4_peak)
+        tf = nums["flops"] / (ms * 1e-3) / 1e12
+        out[name] = {"T": T, "steps": steps, "ms_per_step": ms, "tflops": tf, "tokens_per_s": T / (ms * 1e-3),
+                     "pct_hbm_bw": nums["bytes"] / (ms * 1e-3) / 1e9 / hbm_peak, "pct_fp4_peak": tf / fp4_peak,
+                     "active_experts": nums["active"], "stages_ms": stage_ms,
+                     "l1_roofline": {"bound": roof["bound"], "frac": roof["frac"], "achieved": roof["achieved"],
+                                     "unit": roof["unit"], "kernel_ms": stage_ms["l1_swiglu"],
+                                     "traffic": ncu_traffic(name)},
+                     "clocks": clk}
+        del ws, y, x, logits
+        torch.cuda.empty_cache()
+    return out
 
 
 # ---------------------------------------------------------------- side ops

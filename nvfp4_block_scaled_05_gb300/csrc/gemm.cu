@@ -258,7 +258,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tensormap(&tm_a64);
     prefetch_tensormap(&tm_a128);
     prefetch_tensormap(&tm_b);
-    const uint64_t pol_w = l2_policy_evict_first();  // weights: streamed once
+    // Weights: a weight tile read by one activation tile is streamed once
+    // (evict first); one that several activation tiles of a large expert read
+    // in turn keeps normal priority, so that the activation and output streams
+    // do not push it out of L2 before its last reader.
+    const uint64_t pol_w1 = l2_policy_evict_first();
+    const uint64_t pol_wn = l2_policy_evict_normal();
     const uint64_t pol_a = l2_policy_evict_last();   // activations: reused by every weight tile
     // Copy sources of one tile, decoded one tile ahead of its loads.
     struct TileSrc {
@@ -266,11 +271,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       int box, a_row, b_row, bhalves;
       const uint8_t* sfa;
       const uint8_t* sfb;
+      uint64_t pol_w;
     };
     auto tile_src = [&](int t) {
       int e, nb, mb, rows, ncols;
       sch.decode(t, e, nb, mb, rows, ncols);
       TileSrc c;
+      c.pol_w = tile_start[e + 1] - tile_start[e] > NT ? pol_wn : pol_w1;
       c.tma = rows <= 16 ? &tm_a16 : rows <= 32 ? &tm_a32 : rows <= 64 ? &tm_a64 : &tm_a128;
       c.box = rows <= 16 ? 16 : rows <= 32 ? 32 : rows <= 64 ? 64 : 128;
       c.a_row = pad_off[e] + mb * BM;
@@ -301,14 +308,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           bulk_load(sdst, cur.sfa + kb * 2048, 2048, sffull, pol_a);
           for (int h = 0; h < cur.bhalves; ++h)
             bulk_load(sdst + SFA_BYTES + h * SFA_BYTES, cur.sfb + h * p.sf_rowtile_bytes + kb * 2048, nk * 512,
-                      sffull, pol_w);
+                      sffull, cur.pol_w);
         }
         const uint32_t full = bar_full + 8 * stage;
         // the B box always moves 256 rows; rows past this expert's last weight
         // tile are never multiplied (N=128 MMA), rows past the tensor read zeros
         mbar_arrive_expect_tx(full, cur.box * 128 + BN * 128);
         tma_load_2d(sbase + stage * A_BYTES, cur.tma, full, kb * 128, cur.a_row, pol_a);
-        tma_load_2d(sbase + OFF_B + stage * B_BYTES, &tm_b, full, kb * 128, cur.b_row, pol_w);
+        tma_load_2d(sbase + OFF_B + stage * B_BYTES, &tm_b, full, kb * 128, cur.b_row, cur.pol_w);
         filled |= 1u << stage;
         fill_phase = (fill_phase & ~(1u << stage)) | (phase << stage);
         if (++stage == STAGES) {

@@ -89,6 +89,11 @@ CONFIGS = {
     # prefill / decode, with 32 experts (0.8 GB of weights, still above L2)
     "prefill_small": MoEConfig("prefill_small", T=1024, K=7168, I=2048, E=32, k=8, gs_h=28.0),
     "decode_small": MoEConfig("decode_small", T=16, K=7168, I=2048, E=32, k=8, gs_h=28.0),
+    # profiler-sized skewed case: 32 experts (2 never chosen) with the same
+    # Zipf(1.2) popularity, so the heaviest expert still spans many activation
+    # tiles that share each weight tile (0.8 GB of weights)
+    "skewed_small": MoEConfig("skewed_small", T=2048, K=7168, I=2048, E=32, k=8, routing="zipf",
+                              zipf_s=1.2, n_dead=2, gs_h=28.0),
     # profiler-sized case for the HBM-bound kernels (quantize, combine): 32768
     # routed rows, so the L2 output the combine reads (470 MB) exceeds L2
     "prefill_med": MoEConfig("prefill_med", T=4096, K=7168, I=2048, E=32, k=8, gs_h=28.0),

@@ -177,3 +177,60 @@ def test_fused_dispatch_choice():
     assert not B.moe_forward_uses_fused_dispatch(8193, 256, 8)
     assert not B.moe_forward_uses_fused_dispatch(16384, 256, 8)
     assert B.moe_dispatch_supported(16384, 256, 8)
+
+
+def test_moe_skewed_heaviest_expert_every_tile():
+    """The full-size skewed prefill (T=16384, Zipf(1.2) popularity, 16 experts
+    never chosen): the L2 output rows of the heaviest expert (~15k routed rows,
+    ~117 activation tiles of 128) element by element against the fp64 oracle,
+    16 rows in EVERY one of its activation tiles (each tile's first and last
+    row and 14 seeded others, the ragged last tile included), and every routed
+    row of the three lightest active experts (single-tile groups). The oracle
+    runs only the sampled rows (about 2000 of the 131072), so the case stays
+    within seconds; all columns are compared."""
+    cfg = W.CONFIGS["skewed"]
+    inp = W.moe_inputs(cfg, seed=0, device=DEV)
+    wts = B.prepare_moe_weights(inp["w1"], inp["w2"])
+    gs_h = torch.tensor([cfg.gs_h], dtype=torch.float32, device=DEV)
+    T, K, I, E, k = cfg.T, cfg.K, cfg.I, cfg.E, cfg.k
+    ws = torch.empty(B.moe_forward_workspace_size(T, K, I, E, k), dtype=torch.uint8, device=DEV)
+    B.moe_forward(inp["x"], inp["logits"], wts, k, gs_h, ws=ws)
+    assert B.nvfp4moe_last_device_status() == 0
+    lay = B.moe_forward_workspace_layout(T, K, I, E, k)
+    M = T * k
+    offsets = _ws_view(ws, lay, "offsets", torch.int32, E + 1).cpu().numpy()
+    p2f = _ws_view(ws, lay, "perm_to_flat", torch.int32, M).cpu().numpy()
+    f2p = _ws_view(ws, lay, "flat_to_perm", torch.int32, M).cpu().numpy()
+    counts = np.diff(offsets)
+    heavy = int(np.argmax(counts))
+    light = [int(e) for e in np.argsort(counts, kind="stable") if counts[e] > 0][:3]
+    assert counts[heavy] > 4096 and all(counts[e] <= 128 for e in light)
+    rng = np.random.default_rng(17)
+    rows = []
+    n = int(counts[heavy])
+    for t0 in range(0, n, 128):
+        t1 = min(n, t0 + 128)
+        pick = {t0, t1 - 1} | set(rng.choice(np.arange(t0, t1), min(14, t1 - t0), replace=False).tolist())
+        rows += [int(offsets[heavy]) + r for r in sorted(pick)]
+    for e in light:
+        rows += list(range(int(offsets[e]), int(offsets[e + 1])))
+    tokens = sorted(set(int(p2f[r]) // k for r in rows))
+    x = W.bf16_bits(inp["x"])
+    w1_dev, w2_dev = inp["w1"], inp["w2"]
+    ref = O.moe_forward(x, inp["logits"].cpu().numpy(), lambda e: W.bf16_bits(w1_dev[e]),
+                        lambda e: W.bf16_bits(w2_dev[e]), k, np.float32(cfg.gs_h), tokens=tokens,
+                        experts={heavy, *light}, keep=True)
+    assert np.array_equal(ref["offsets"], offsets)
+    out = _ws_view(ws, lay, "out", torch.bfloat16, M * K).view(M, K)
+    want_rows = set(rows)
+    idx, want = [], []
+    for (t, j), d in ref["inter"].items():
+        r = int(f2p[t * k + j])
+        if r in want_rows:
+            idx.append(r)
+            want.append(d["o"])
+    assert len(idx) == len(want_rows)
+    got = out[torch.tensor(idx, device=DEV)].float().cpu().numpy()
+    want = np.array(want)
+    assert_close_tol(got, want, "skewed heaviest expert %d and experts %s" % (heavy, light))
+    assert cosine(got, want) >= 0.9995

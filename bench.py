@@ -61,6 +61,9 @@ def parse_args():
                          "kernels); static: moe_forward_static (one fused front kernel, gs_x "
                          "pre-computed once)")
     ap.add_argument("--graph", action="store_true", help="replay the step as a captured CUDA graph")
+    ap.add_argument("--gemm-mode", type=int, default=0, choices=[0, 1],
+                    help="grouped-GEMM kernel: 0 one CTA per tile (default), 1 2-SM pairs (clusters of two CTAs "
+                         "sharing one MMA) where N %% 256 == 0")
     ap.add_argument("--op", default="moe", choices=["moe", "qnorm_rope", "linear"],
                     help="moe: the expert forward (default); qnorm_rope: the fused RMS norm + RoPE + "
                          "NVFP4 quantization of attention-head rows; linear: the shared-expert NVFP4 "
@@ -426,6 +429,7 @@ def run_ours(args, cfg):
         pg = dist
     from nvfp4_block_scaled_05_gb300 import binding as B
     from nvfp4_block_scaled_05_gb300 import workloads as W
+    B.nvfp4moe_set_gemm_mode(args.gemm_mode)
 
     # inputs: replicated weights (same seed on every rank), per-rank tokens
     inp = W.moe_inputs(cfg, seed=args.seed, device=dev, weights=True)
@@ -621,6 +625,7 @@ def run_ours(args, cfg):
                              ("fused dispatch kernel (gs_x computed every step)" if fused_front else
                               "route, permute and quantize kernels (gs_x computed every step)")),
                    "cuda_graph": bool(args.graph),
+                   "gemm_kernel": "2-SM pairs" if args.gemm_mode == 1 else "one CTA per tile",
                    "l2": "inputs larger than L2: %.2f GB of expert weights streamed every step"
                          % (nums["bytes"] / 1e9)},
         "tokens_per_s": tokens_s,

@@ -491,6 +491,17 @@ void nvfp4moe_set_wait_limit_ns(uint64_t ns);
  * afterwards. */
 void nvfp4moe_set_test_stall(int on);
 
+/* Which grouped-GEMM kernel the GEMM entry points launch (host only; affects
+ * launches made afterwards). 0 (default): one CTA per tile of 128 activation
+ * rows x 256 weight rows. 1: a tile of 256 activation rows x 256 weight rows
+ * on a pair of SMs (a thread-block cluster of two CTAs sharing one 2-SM
+ * tcgen05 MMA, each CTA loading its 128 activation rows and half of the
+ * weight tile) whenever N % 256 == 0, else one CTA per tile. Both give the
+ * same results bit for bit; on this GB300 the pairs measured slower (their
+ * cross-SM hand-offs lengthen the load round trip that bounds both kernels),
+ * so they are not the default. Returns NVFP4MOE_OK or NVFP4MOE_ERR_INVALID. */
+int nvfp4moe_set_gemm_mode(int mode);
+
 /* Number of streaming multiprocessors of the current device (grid size of the
  * persistent GEMM kernels). Host only. */
 int nvfp4moe_num_sms(void);

@@ -79,6 +79,7 @@ _SIGS = {
     "nvfp4moe_set_wait_limit_ns": (None, [ctypes.c_uint64]),
     "nvfp4moe_set_test_stall": (None, [_int]),
     "nvfp4moe_num_sms": (_int, []),
+    "nvfp4moe_set_gemm_mode": (_int, [_int]),
 }
 
 _lib = None
@@ -180,6 +181,11 @@ def nvfp4_interleave_gate_up(codes, sf, two_i, K, sf_layout=NVFP4_SF_ROWMAJOR, i
     _check(lib().nvfp4_interleave_gate_up(_ptr(codes), _ptr(sf), batch, two_i, K, sf_layout, int(bool(inverse)),
                                           _ptr(co), _ptr(so), _stream()), "nvfp4_interleave_gate_up")
     return co, so
+
+
+def nvfp4moe_set_gemm_mode(mode):
+    """0: one CTA per tile (default); 1: the 2-SM pair kernel where N % 256 == 0."""
+    _check(lib().nvfp4moe_set_gemm_mode(int(mode)), "nvfp4moe_set_gemm_mode")
 
 
 def nvfp4moe_num_sms():

@@ -107,10 +107,14 @@ __device__ __forceinline__ uint32_t e2m1x8(const float (&q)[8]) {
 }
 
 // RN(a / s) for an E4M3 block scale s > 0, given rcp = RN(1 / s): the product
-// with the reciprocal, corrected by one FMA on its exact remainder. Equal to the
-// correctly rounded quotient bit for bit for every f32 a and every E4M3 s
-// (checked exhaustively on the host, tests/fma_division_check.c); the sign is
-// copied from a so that a = -0 gives -0.
+// with the reciprocal, corrected by one FMA on its exact remainder. This is the
+// final correction step of P. Markstein's FMA-based division ("Computation of
+// elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34(1), 1990; also "IA-64 and Elementary Functions", 2000): with an
+// exact remainder r = a - q0*s (one FMA) the corrected q0 + r*rcp rounds to the
+// correctly rounded quotient. Equal to that quotient bit for bit for every f32
+// a and every E4M3 s (checked exhaustively on the host,
+// tests/fma_division_check.c); the sign is copied from a so that a = -0 gives -0.
 __device__ __forceinline__ float div_by_scale(float a, float s, float rcp) {
   const float q0 = __fmul_rn(a, rcp);
   const float r = __fmaf_rn(-q0, s, a);
@@ -436,6 +440,105 @@ __device__ __forceinline__ void tc_ld64_wait(uint32_t taddr, uint32_t (&r)[64]) 
         "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
         "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
       : "r"(taddr)
+      : "memory");
+}
+
+// ---- thread-block clusters of two CTAs (the 2-SM MMA pairs)
+
+// Rank of this CTA in its cluster.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of both CTAs: arrive (release) and wait (acquire) on the
+// cluster's hardware barrier.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address in the shared::cluster window of the variable at shared::cta
+// address `addr` in the cluster's CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+// Arrive (release at cluster scope) on an mbarrier of another CTA of the
+// cluster, given its shared::cluster address.
+__device__ __forceinline__ void mbar_remote_arrive(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// The same with relaxed ordering: no release fence, so it costs the issuing
+// thread almost nothing (a release at cluster scope measured ~0.4 us per
+// arrive). Used where what the arrive announces was already observed complete
+// through a local barrier (copies landed, tensor-memory stores or loads waited
+// for), so there is nothing left for a release to order.
+__device__ __forceinline__ void mbar_remote_arrive_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// Store a 32-bit word into another CTA's shared memory (shared::cluster address).
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
+// Parity wait with acquire at cluster scope (for barriers a peer CTA arrives on).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Tensor memory of a CTA pair: one warp of EACH of the two CTAs executes the
+// allocation (and later the deallocation); both receive the same address.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// Arrive on the mbarrier at the same shared-memory offset in every CTA of
+// `cta_mask` once the pair MMAs this thread issued so far are done.
+__device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
+      : "memory");
+}
+
+// The same, on this CTA's own mbarrier only.
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// The 2-SM form of tc_mma_nvf4, issued by one thread of the pair's even CTA:
+// M = 256 rows, the first 128 from the even CTA's shared memory and the other
+// 128 from the odd CTA's (same offsets), N split the same way for B; each CTA
+// receives its 128 rows of D in its own tensor memory, and each reads its own
+// A scales and the B scales from its own tensor memory.
+__device__ __forceinline__ void tc_mma_nvf4_pair(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                 uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], "
+      "[%6], p;\n\t}" ::"r"(d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
       : "memory");
 }
 

@@ -54,35 +54,43 @@ namespace {
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 256;                       // K elements per stage
-constexpr int STAGES = 4;
 constexpr int kScaleWarps = 4;
 constexpr int kEpiWarps = 8;
 constexpr int kFirstEpiWarp = 2 + kScaleWarps;
 constexpr int kThreads = 32 * (2 + kScaleWarps + kEpiWarps);
 constexpr int A_BYTES = BM * BK / 2;          // 16 KB
-constexpr int B_BYTES = BN * BK / 2;          // 32 KB
 constexpr int SFA_BYTES = 4 * 512;            // 4 scale atoms (K=256) of 128 rows
 constexpr int SF_BYTES = 3 * SFA_BYTES;       // SFA, then SFB's two 128-row halves
-constexpr int OFF_B = STAGES * A_BYTES;
-constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
-constexpr int OFF_BAR = OFF_SF + STAGES * SF_BYTES;
 constexpr int kScaleThreads = 32 * 4;         // the scale warps
-constexpr int OFF_MISC = OFF_BAR + 256;
-constexpr int OFF_SCHED = OFF_MISC + 256;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COLS = BN;             // one f32 accumulator of 256 columns
-// Scale slots after the accumulator. A TMEM store of n columns starts on a
-// multiple of n, so each stage's 32 SFB columns (k-step kk in columns 8kk ..
-// 8kk+7) start on a multiple of 32, and the SFA slots (quadrant q: k-step kk in
-// column 4kk + q, one-column stores) follow all of them.
-constexpr uint32_t SFB_TMEM0 = ACC_COLS;
 constexpr uint32_t SFB_SLOT = 32;
-constexpr uint32_t SFA_TMEM0 = SFB_TMEM0 + STAGES * SFB_SLOT;
 constexpr uint32_t SFA_SLOT = 16;
 constexpr uint64_t kDrainLimitNs = 1000000000ull;
 
-static_assert(SFA_TMEM0 + STAGES * SFA_SLOT <= TMEM_COLS, "tensor memory budget");
-static_assert(OFF_SCHED + 8 * 1025 + 1024 <= 232448, "shared memory budget");
+// Shared- and tensor-memory plan of one CTA. kPair: the CTA is one half of a
+// 2-SM pair and holds only its 128 of the tile's 256 weight rows, which frees
+// shared memory for a fifth stage.
+template <bool kPair>
+struct Cfg {
+  static constexpr int STAGES = kPair ? 5 : 4;
+  static constexpr int B_ROWS = kPair ? BN / 2 : BN;    // weight rows this CTA loads per tile
+  static constexpr int B_BYTES = B_ROWS * BK / 2;       // 16 / 32 KB
+  static constexpr int OFF_B = STAGES * A_BYTES;
+  static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
+  static constexpr int OFF_BAR = OFF_SF + STAGES * SF_BYTES;
+  static constexpr int OFF_MISC = OFF_BAR + (kPair ? 512 : 256);
+  static constexpr int OFF_SCHED = OFF_MISC + 256;
+  // Scale slots after the accumulator. A TMEM store of n columns starts on a
+  // multiple of n, so each stage's 32 SFB columns (k-step kk in columns 8kk ..
+  // 8kk+7) start on a multiple of 32, and the SFA slots (quadrant q: k-step kk
+  // in column 4kk + q, one-column stores) follow all of them.
+  static constexpr uint32_t SFB_TMEM0 = ACC_COLS;
+  static constexpr uint32_t SFA_TMEM0 = SFB_TMEM0 + STAGES * SFB_SLOT;
+  static_assert(SFA_TMEM0 + STAGES * SFA_SLOT <= TMEM_COLS, "tensor memory budget");
+  static_assert(OFF_SCHED + 8 * 1025 + 1024 <= 232448, "shared memory budget");
+  static_assert((kPair ? 7 * STAGES + 6 : 6 * STAGES + 4) * 8 <= OFF_MISC - OFF_BAR, "barrier area");
+};
 
 struct Params {
   const uint8_t* a_sf;
@@ -110,14 +118,21 @@ struct Params {
   int test_stall;             // test hook: the MMA issuer first waits on a barrier nobody arrives on
 };
 
+// Work units, ordered expert-major, then weight tile, then activation tile(s).
+// A unit is one 128-row activation tile x one 256-row weight tile, or with
+// pairs two consecutive activation tiles of the expert (the even CTA takes the
+// first, the odd CTA the second, which may not exist) x one weight tile.
 struct Sched {
-  const int32_t* tile_start;  // [E+1] first tile of each expert
+  const int32_t* tile_start;  // [E+1] first unit of each expert
   const int32_t* pad_off;     // [E+1] padded first row of each expert
   const int32_t* offsets;     // [E+1] compact first row of each expert
   int E;
   int NT;                     // weight tiles per expert
   int N;
-  __device__ __forceinline__ void decode(int t, int& e, int& nb, int& mb, int& rows, int& ncols) const {
+  int pair;                   // 1: units of two activation tiles
+  // rows <= 0: no activation tile of this CTA in the unit (the odd CTA of a
+  // pair whose expert has an odd number of activation tiles)
+  __device__ __forceinline__ void decode(int t, int rank, int& e, int& nb, int& mb, int& rows, int& ncols) const {
     int lo = 0, hi = E - 1;
     while (lo < hi) {  // largest e with tile_start[e] <= t
       const int mid = (lo + hi + 1) >> 1;
@@ -125,28 +140,34 @@ struct Sched {
       else hi = mid - 1;
     }
     e = lo;
-    const int mt = (tile_start[e + 1] - tile_start[e]) / NT;
+    const int per = (tile_start[e + 1] - tile_start[e]) / NT;   // units per weight tile
     const int local = t - tile_start[e];
-    nb = local / mt;
-    mb = local - nb * mt;
+    nb = local / per;
+    const int m = local - nb * per;
+    mb = pair ? 2 * m + rank : m;
     const int cnt = offsets[e + 1] - offsets[e];
     rows = min(BM, cnt - mb * BM);
     ncols = min(BN, N - nb * BN);   // 256, or 128 for the last tile when N % 256 == 128
   }
 };
 
-// Bounded wait. Returns false on timeout (after raising the abort flag and
-// the device status) or when another role has aborted.
+// Bounded wait. Returns false on timeout (after raising the abort flag, the
+// pair peer's abort flag when peer_abort != 0, and the device status) or when
+// another role has aborted. kCluster: the barrier is arrived on from the pair
+// peer (acquire at cluster scope).
+template <bool kCluster = false>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                             uint64_t limit_ns, int* status, int site) {
-  if (mbar_try_wait(bar, parity)) return true;
+                                             uint64_t limit_ns, int* status, int site, uint32_t peer_abort = 0) {
+  auto probe = [&]() { return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+  if (probe()) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (probe()) return true;
     if ((it & 15u) == 0) {
       if (*abort_flag) return false;
       if (global_timer_ns() - t0 > limit_ns) {
         *abort_flag = 1;
+        if (peer_abort) st_shared_cluster_u32(peer_abort, 1u);
         if (atomicCAS(&status[0], 0, NVFP4MOE_ERR_DEVICE_TIMEOUT) == 0) status[1] = site;
         return false;
       }
@@ -155,9 +176,10 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
 }
 
 // Wait used while shutting down: ignores the abort flag, fixed bound.
+template <bool kCluster = false>
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!(kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity))) {
     if (global_timer_ns() - t0 > kDrainLimitNs) return;
   }
 }
@@ -166,19 +188,21 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 // (a few ulp; h is requantized to 4 bits right after).
 __device__ __forceinline__ float silu(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
-template <bool kSwiGLU>
+template <bool kSwiGLU, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a16,
                         const __grid_constant__ CUtensorMap tm_a32,
                         const __grid_constant__ CUtensorMap tm_a64,
                         const __grid_constant__ CUtensorMap tm_a128,
                         const __grid_constant__ CUtensorMap tm_b, const Params p) {
+  using C = Cfg<kPair>;
+  constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t sbase = smem_addr(smem);
-  const uint32_t bar_full = sbase + OFF_BAR;               // STAGES x 8 bytes each
+  const uint32_t bar_full = sbase + C::OFF_BAR;            // STAGES x 8 bytes each
   const uint32_t bar_sfready = bar_full + STAGES * 8;
   const uint32_t bar_empty = bar_sfready + STAGES * 8;
   const uint32_t bar_accf = bar_empty + STAGES * 8;
@@ -188,38 +212,56 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_sfland = bar_never + 8;               // STAGES: a stage's scale atoms landed
   const uint32_t bar_sfcons = bar_sfland + STAGES * 8;     // STAGES: its scale atoms read by all scale warps
   const uint32_t bar_sffull = bar_sfcons + STAGES * 8;     // STAGES: scale atoms copied by the producer landed
+  // pairs: the odd CTA's stage s is loaded and its scales stored (arrived on
+  // from the odd CTA, used by the even CTA's MMA issuer); the odd CTA's
+  // epilogue released the accumulator; the exit handshake
+  const uint32_t bar_peer_full = bar_sffull + STAGES * 8;  // STAGES
+  const uint32_t bar_peer_acce = bar_peer_full + STAGES * 8;
+  const uint32_t bar_exit = bar_peer_acce + 8;
   // Scale atoms reach shared memory either as bulk copies from the TMA
   // producer (L1: its epilogue's register spills use the load path) or as
   // cp.async copies from the scale warps (L2), whose load path adds to the
   // TMA engine's bandwidth.
   constexpr bool kScalesByTMA = kSwiGLU;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
-  int32_t* tile_start = reinterpret_cast<int32_t*>(smem + OFF_SCHED);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  int32_t* tile_start = reinterpret_cast<int32_t*>(smem + C::OFF_SCHED);
   int32_t* pad_off = tile_start + (p.E + 1);
   const int E = p.E, NT = (p.N + BN - 1) / BN;
+  // pairs: rank 0 (the even CTA) issues the MMAs of both
+  const int rank = kPair ? (int)cluster_ctarank() : 0;
+  const int first_unit = kPair ? (int)blockIdx.x / 2 : (int)blockIdx.x;
+  const int unit_stride = kPair ? (int)gridDim.x / 2 : (int)gridDim.x;
+  const uint32_t peer_abort = kPair ? mapa_shared(smem_addr(smem + C::OFF_MISC + 4), rank ^ 1) : 0u;
 
-  // --- schedule: per expert its activation tiles (ceil(n_e/128)), prefix sums
+  // --- schedule: per expert its units (ceil(n_e/128) activation tiles, or
+  //     ceil of half of that with pairs, per weight tile), prefix sums
   if (warp == 0) {
-    int carry = 0;
+    int carry = 0, carry_rows = 0;
     for (int base = 0; base < E; base += 32) {
       const int e = base + lane;
       const int mt = e < E ? (p.offsets[e + 1] - p.offsets[e] + BM - 1) / BM : 0;
-      int incl = mt;
+      const int mu = kPair ? (mt + 1) / 2 : mt;
+      int incl = mu, incl_rows = mt;
 #pragma unroll
       for (int d = 1; d < 32; d <<= 1) {
         const int y = __shfl_up_sync(0xFFFFFFFFu, incl, d);
-        if (lane >= d) incl += y;
+        const int yr = __shfl_up_sync(0xFFFFFFFFu, incl_rows, d);
+        if (lane >= d) {
+          incl += y;
+          incl_rows += yr;
+        }
       }
       if (e < E) {
-        tile_start[e] = (carry + incl - mt) * NT;
-        pad_off[e] = (carry + incl - mt) * BM;
+        tile_start[e] = (carry + incl - mu) * NT;
+        pad_off[e] = (carry_rows + incl_rows - mt) * BM;
       }
       carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+      carry_rows += __shfl_sync(0xFFFFFFFFu, incl_rows, 31);
     }
     if (lane == 0) {
       tile_start[E] = carry * NT;
-      pad_off[E] = carry * BM;
+      pad_off[E] = carry_rows * BM;
     }
   }
   if (tid == 32) {
@@ -230,26 +272,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_sfcons + 8 * s, kScaleWarps);
       mbar_init(bar_sffull + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
+      if constexpr (kPair) mbar_init(bar_peer_full + 8 * s, 1);
     }
     mbar_init(bar_accf, 1);
     mbar_init(bar_acce, kEpiWarps * 32);
     mbar_init(bar_aux, 1);
     mbar_init(bar_never, 1);
+    if constexpr (kPair) {
+      mbar_init(bar_peer_acce, 1);
+      mbar_init(bar_exit, 1);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_addr(tmem_slot), TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (kPair) {
+      tmem_alloc_pair(smem_addr(tmem_slot), TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_addr(tmem_slot), TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (kPair) cluster_sync_all();   // the peer's barriers exist before anyone arrives on them
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int total = tile_start[E];
-  const Sched sch{tile_start, pad_off, p.offsets, E, NT, p.N};
+  const Sched sch{tile_start, pad_off, p.offsets, E, NT, p.N, kPair ? 1 : 0};
   const int ksteps = p.K / 64;
   const int kblocks = (ksteps + 3) / 4;
+  const int my_units = first_unit < total ? (total - 1 - first_unit) / unit_stride + 1 : 0;
 
   if (warp == 0 && lane == 0) {
     // ---------------------------------------------------------------- producer
@@ -258,30 +312,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tensormap(&tm_a64);
     prefetch_tensormap(&tm_a128);
     prefetch_tensormap(&tm_b);
-    // Weights: a weight tile read by one activation tile is streamed once
-    // (evict first); one that several activation tiles of a large expert read
-    // in turn keeps normal priority, so that the activation and output streams
-    // do not push it out of L2 before its last reader.
+    // Weights: a weight tile read by one unit is streamed once (evict first);
+    // one that several units of a large expert read in turn keeps normal
+    // priority, so that the activation and output streams do not push it out
+    // of L2 before its last reader.
     const uint64_t pol_w1 = l2_policy_evict_first();
     const uint64_t pol_wn = l2_policy_evict_normal();
     const uint64_t pol_a = l2_policy_evict_last();   // activations: reused by every weight tile
-    // Copy sources of one tile, decoded one tile ahead of its loads.
+    // Copy sources of one unit, decoded one unit ahead of its loads.
     struct TileSrc {
       const CUtensorMap* tma;
       int box, a_row, b_row, bhalves;
+      bool has_a;
       const uint8_t* sfa;
       const uint8_t* sfb;
       uint64_t pol_w;
     };
     auto tile_src = [&](int t) {
       int e, nb, mb, rows, ncols;
-      sch.decode(t, e, nb, mb, rows, ncols);
+      sch.decode(t, rank, e, nb, mb, rows, ncols);
       TileSrc c;
       c.pol_w = tile_start[e + 1] - tile_start[e] > NT ? pol_wn : pol_w1;
+      c.has_a = rows > 0;
       c.tma = rows <= 16 ? &tm_a16 : rows <= 32 ? &tm_a32 : rows <= 64 ? &tm_a64 : &tm_a128;
       c.box = rows <= 16 ? 16 : rows <= 32 ? 32 : rows <= 64 ? 64 : 128;
       c.a_row = pad_off[e] + mb * BM;
-      c.b_row = e * p.N + nb * BN;
+      c.b_row = e * p.N + nb * BN + rank * C::B_ROWS;
       c.bhalves = ncols / 128;
       c.sfa = p.a_sf + (int64_t)(c.a_row / BM) * p.a_sf_rowtile_bytes;
       c.sfb = p.b_sf + (int64_t)e * p.b_sf_expert_bytes + (int64_t)(nb * 2) * p.sf_rowtile_bytes;
@@ -290,32 +346,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t stage = 0, phase = 0, filled = 0, fill_phase = 0;
     bool ok = true;
     TileSrc cur{}, nxt{};
-    if (blockIdx.x < total) cur = tile_src(blockIdx.x);
-    for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-      const bool has_next = t + (int)gridDim.x < total;
-      if (has_next) nxt = tile_src(t + gridDim.x);
+    if (first_unit < total) cur = tile_src(first_unit);
+    for (int t = first_unit; ok && t < total; t += unit_stride) {
+      const bool has_next = t + unit_stride < total;
+      if (has_next) nxt = tile_src(t + unit_stride);
       for (int kb = 0; kb < kblocks; ++kb) {
-        if (!wait_bounded(bar_empty + 8 * stage, phase ^ 1, abort_flag, p.wait_limit_ns, p.status, 1)) {
+        if (!wait_bounded(bar_empty + 8 * stage, phase ^ 1, abort_flag, p.wait_limit_ns, p.status, 1, peer_abort)) {
           ok = false;
           break;
         }
         if constexpr (kScalesByTMA) {
           const int nk = min(4, ksteps - kb * 4);
           const uint32_t sffull = bar_sffull + 8 * stage;
-          const uint32_t sdst = sbase + OFF_SF + stage * SF_BYTES;
+          const uint32_t sdst = sbase + C::OFF_SF + stage * SF_BYTES;
           // the activation scales of a stage are 2048 bytes whatever the K tail
-          mbar_arrive_expect_tx(sffull, 2048 + cur.bhalves * nk * 512);
-          bulk_load(sdst, cur.sfa + kb * 2048, 2048, sffull, pol_a);
+          mbar_arrive_expect_tx(sffull, (cur.has_a ? 2048 : 0) + cur.bhalves * nk * 512);
+          if (cur.has_a) bulk_load(sdst, cur.sfa + kb * 2048, 2048, sffull, pol_a);
           for (int h = 0; h < cur.bhalves; ++h)
             bulk_load(sdst + SFA_BYTES + h * SFA_BYTES, cur.sfb + h * p.sf_rowtile_bytes + kb * 2048, nk * 512,
                       sffull, cur.pol_w);
         }
         const uint32_t full = bar_full + 8 * stage;
-        // the B box always moves 256 rows; rows past this expert's last weight
-        // tile are never multiplied (N=128 MMA), rows past the tensor read zeros
-        mbar_arrive_expect_tx(full, cur.box * 128 + BN * 128);
-        tma_load_2d(sbase + stage * A_BYTES, cur.tma, full, kb * 128, cur.a_row, pol_a);
-        tma_load_2d(sbase + OFF_B + stage * B_BYTES, &tm_b, full, kb * 128, cur.b_row, cur.pol_w);
+        // the B box always moves B_ROWS rows; rows past this expert's last
+        // weight tile are never multiplied (N=128 MMA), rows past the tensor
+        // read zeros
+        mbar_arrive_expect_tx(full, (cur.has_a ? cur.box * 128 : 0) + C::B_ROWS * 128);
+        if (cur.has_a) tma_load_2d(sbase + stage * A_BYTES, cur.tma, full, kb * 128, cur.a_row, pol_a);
+        tma_load_2d(sbase + C::OFF_B + stage * C::B_BYTES, &tm_b, full, kb * 128, cur.b_row, cur.pol_w);
         filled |= 1u << stage;
         fill_phase = (fill_phase & ~(1u << stage)) | (phase << stage);
         if (++stage == STAGES) {
@@ -325,36 +382,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       cur = nxt;
     }
-    // copies still in flight complete before the CTA may exit
-    if (!ok)
+    if (!ok) {
+      // copies still in flight complete before the CTA may exit
       for (int s = 0; s < STAGES; ++s)
         if ((filled >> s) & 1u) {
           drain_wait(bar_full + 8 * s, (fill_phase >> s) & 1u);
           if constexpr (kScalesByTMA) drain_wait(bar_sffull + 8 * s, (fill_phase >> s) & 1u);
         }
+    } else if constexpr (kPair) {
+      // every stage's last use released by the even CTA's MMAs (whose commits
+      // arrive on this CTA's barriers) before the CTA may exit
+      for (int i = 0; i < STAGES; ++i) {
+        if (!wait_bounded(bar_empty + 8 * stage, phase ^ 1, abort_flag, p.wait_limit_ns, p.status, 10, peer_abort))
+          break;
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
   } else if (warp >= 2 && warp < kFirstEpiWarp) {
     // ---------------------------------------------------------------- scale warps
     // The scale atoms travel through the load path (cp.async), not the TMA
     // engine that the code tiles saturate: the 128 scale threads copy a stage's
-    // atoms (up to 6 KB) into a 4-slot shared-memory ring up to STAGES stages
-    // ahead; a slot is refilled once all four warps have read it. Per stage,
-    // each warp then stores its quadrant's scales into the stage's TMEM slot.
+    // atoms (up to 6 KB) into a STAGES-slot shared-memory ring up to STAGES
+    // stages ahead; a slot is refilled once all four warps have read it. Per
+    // stage, each warp then stores its quadrant's scales into the stage's TMEM
+    // slot. A pair CTA without an activation tile in the unit stores zero A
+    // scales (its rows of the MMA are discarded).
     const int q = warp & 3;                               // TMEM lane quadrant of this warp
     const uint32_t lanes = static_cast<uint32_t>(q * 32) << 16;
     const int st_id = (warp - 2) * 32 + lane;              // 0..127 among the scale threads
-    const int my_tiles = blockIdx.x < total ? (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-    const int nstages = my_tiles * kblocks;
-    // copy cursor: tile, k-block and the tile's scale sources
-    int ct = blockIdx.x, ckb = 0;
+    const int nstages = my_units * kblocks;
+    // copy cursor: unit, k-block and the unit's scale sources
+    int ct = first_unit, ckb = 0;
     const uint8_t* csfa = nullptr;
     const uint8_t* csfb = nullptr;
-    bool ctwo = false;
+    bool ctwo = false, chas_a = true;
     auto load_tile = [&](int t) {
       int e, nb, mb, rows, ncols;
-      sch.decode(t, e, nb, mb, rows, ncols);
+      sch.decode(t, rank, e, nb, mb, rows, ncols);
       csfa = p.a_sf + (int64_t)((pad_off[e] + mb * BM) / BM) * p.a_sf_rowtile_bytes;
       csfb = p.b_sf + (int64_t)e * p.b_sf_expert_bytes + (int64_t)(nb * 2) * p.sf_rowtile_bytes;
       ctwo = ncols > 128;
+      chas_a = rows > 0;
     };
     if (!kScalesByTMA && nstages > 0) load_tile(ct);
     bool ok = true;
@@ -362,17 +433,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto issue = [&]() -> bool {
       if constexpr (kScalesByTMA) return true;           // the producer copies the atoms
       const int slot = gc % STAGES, use = gc / STAGES;
-      if (use > 0 && !wait_bounded(bar_sfcons + 8 * slot, (use - 1) & 1, abort_flag, p.wait_limit_ns, p.status, 5))
+      if (use > 0 &&
+          !wait_bounded(bar_sfcons + 8 * slot, (use - 1) & 1, abort_flag, p.wait_limit_ns, p.status, 5, peer_abort))
         return false;
       const int nk = min(4, ksteps - ckb * 4);
-      const uint32_t dst = sbase + OFF_SF + slot * SF_BYTES;
+      const uint32_t dst = sbase + C::OFF_SF + slot * SF_BYTES;
       // 384 chunks of 16 bytes: the activation scales (128 rows x 16 bytes),
       // then the weight scale atoms of halves 0 and 1 (128 each); weight atoms
       // past a K tail, or of a missing second half, are not copied
 #pragma unroll
       for (int i = 0; i < 3; ++i) {
         const int c = st_id + kScaleThreads * i;           // region i, chunk st_id
-        const bool live = i == 0 || (st_id < nk * 32 && (i < 2 || ctwo));
+        const bool live = i == 0 ? chas_a : (st_id < nk * 32 && (i < 2 || ctwo));
         if (live) {
           const uint8_t* src = i == 0 ? csfa + ckb * 2048 + st_id * 16
                                       : csfb + (int64_t)(i - 1) * p.sf_rowtile_bytes + ckb * 2048 + st_id * 16;
@@ -383,19 +455,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++gc;
       if (++ckb == kblocks) {
         ckb = 0;
-        ct += gridDim.x;
+        ct += unit_stride;
         if (ct < total) load_tile(ct);
       }
       return true;
     };
+    bool use_has_a = true;                                // the consumed unit has this CTA's activation tile
     for (int g = 0; ok && g < nstages; ++g) {
+      if constexpr (kPair) {
+        if (g % kblocks == 0) {
+          int e, nb, mb, rows, ncols;
+          sch.decode(first_unit + (g / kblocks) * unit_stride, rank, e, nb, mb, rows, ncols);
+          use_has_a = rows > 0;
+        }
+      }
       if constexpr (!kScalesByTMA) {
         while (ok && gc < nstages && gc < g + STAGES) ok = __all_sync(0xFFFFFFFFu, issue());
         if (!ok) break;
       }
       const int slot = g % STAGES, use = g / STAGES;
       ok = wait_bounded((kScalesByTMA ? bar_sffull : bar_sfland) + 8 * slot, use & 1, abort_flag,
-                        p.wait_limit_ns, p.status, 5);
+                        p.wait_limit_ns, p.status, 5, peer_abort);
       ok = __all_sync(0xFFFFFFFFu, ok);
       if (!ok) break;
       // Activation scales: row r's 16 blocks are the 16 bytes at r * 16, the
@@ -403,12 +483,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // of a 512-byte atom holds rows lane, lane+32, lane+64, lane+96 (4 bytes
       // each, one per 16-element block). Slots past a K tail (and the second
       // half of a 128-column tile) hold stale bytes the MMAs never read.
-      const uint8_t* ssfa = smem + OFF_SF + slot * SF_BYTES + (q * 32 + lane) * 16;
-      const uint8_t* ssfb = smem + OFF_SF + slot * SF_BYTES + SFA_BYTES + lane * 16;
+      const uint8_t* ssfa = smem + C::OFF_SF + slot * SF_BYTES + (q * 32 + lane) * 16;
+      const uint8_t* ssfb = smem + C::OFF_SF + slot * SF_BYTES + SFA_BYTES + lane * 16;
       uint32_t a[4], b[32];
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
-        a[kk] = *reinterpret_cast<const uint32_t*>(ssfa + kk * 4);      // row 32q + lane
+        a[kk] = use_has_a ? *reinterpret_cast<const uint32_t*>(ssfa + kk * 4) : 0u;   // row 32q + lane
         // B rows lane+32j, j = 0..3 (first 128 rows) and 4..7 (second 128 rows)
         const uint4 lo = *reinterpret_cast<const uint4*>(ssfb + kk * 512);
         const uint4 hi = *reinterpret_cast<const uint4*>(ssfb + SFA_BYTES + kk * 512);
@@ -420,14 +500,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(bar_sfcons + 8 * slot);
         // the TMEM slot is free once the MMAs of its previous use completed
         // (with producer copies, their landing already implies it)
-        ok = wait_bounded(bar_empty + 8 * slot, (use & 1) ^ 1, abort_flag, p.wait_limit_ns, p.status, 5);
+        ok = wait_bounded(bar_empty + 8 * slot, (use & 1) ^ 1, abort_flag, p.wait_limit_ns, p.status, 5, peer_abort);
         ok = __all_sync(0xFFFFFFFFu, ok);
         if (!ok) break;
       }
-      const uint32_t sfa_t = tmem + lanes + SFA_TMEM0 + slot * SFA_SLOT + q;
+      const uint32_t sfa_t = tmem + lanes + C::SFA_TMEM0 + slot * SFA_SLOT + q;
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) tc_st1(sfa_t + 4 * kk, a[kk]);
-      tc_st32(tmem + lanes + SFB_TMEM0 + slot * SFB_SLOT, b);
+      tc_st32(tmem + lanes + C::SFB_TMEM0 + slot * SFB_SLOT, b);
       tc_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -435,67 +515,115 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // this thread's copies land before the CTA may exit
     cp_async_wait_all();
-  } else if (warp == 1 && lane == 0) {
+  } else if (warp == 1 && lane == 0 && rank == 0) {
     // ---------------------------------------------------------------- MMA issuer
     uint32_t stage = 0, phase = 0, aphase = 0;
     bool ok = true, issued = false;
     // Only the weight-tile width changes between tiles, and only when N is not a
     // multiple of 256; otherwise the issuer never decodes a tile (decoding reads
     // global memory, which would leave the tensor pipe idle at tile boundaries).
-    const bool uniform_n = p.N % BN == 0;
+    // Pairs always have N % 256 == 0.
+    const bool uniform_n = kPair || p.N % BN == 0;
     const uint64_t adesc0 = sdesc_kmajor_sw128(sbase);
-    const uint64_t bdesc0 = sdesc_kmajor_sw128(sbase + OFF_B);
-    if (p.test_stall && blockIdx.x < total)
-      ok = wait_bounded(bar_never, 0, abort_flag, p.wait_limit_ns, p.status, 6);
-    for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-      uint32_t idesc = idesc_nvf4(BM, BN);
+    const uint64_t bdesc0 = sdesc_kmajor_sw128(sbase + C::OFF_B);
+    if (p.test_stall && first_unit < total)
+      ok = wait_bounded(bar_never, 0, abort_flag, p.wait_limit_ns, p.status, 6, peer_abort);
+    for (int t = first_unit; ok && t < total; t += unit_stride) {
+      uint32_t idesc = idesc_nvf4(kPair ? 2 * BM : BM, BN);
       if (!uniform_n) {
         int e, nb, mb, rows, ncols;
-        sch.decode(t, e, nb, mb, rows, ncols);
+        sch.decode(t, 0, e, nb, mb, rows, ncols);
         idesc = idesc_nvf4(BM, ncols);
       }
-      if (!wait_bounded(bar_acce, aphase ^ 1, abort_flag, p.wait_limit_ns, p.status, 2)) {
+      if (!wait_bounded(bar_acce, aphase ^ 1, abort_flag, p.wait_limit_ns, p.status, 2, peer_abort) ||
+          (kPair && !wait_bounded<true>(bar_peer_acce, aphase ^ 1, abort_flag, p.wait_limit_ns, p.status, 11,
+                                        peer_abort))) {
         ok = false;
         break;
       }
       tc_fence_after();
       for (int kb = 0; kb < kblocks; ++kb) {
-        if (!wait_bounded(bar_sfready + 8 * stage, phase, abort_flag, p.wait_limit_ns, p.status, 3) ||
-            !wait_bounded(bar_full + 8 * stage, phase, abort_flag, p.wait_limit_ns, p.status, 7)) {
+        if (!wait_bounded(bar_sfready + 8 * stage, phase, abort_flag, p.wait_limit_ns, p.status, 3, peer_abort) ||
+            !wait_bounded(bar_full + 8 * stage, phase, abort_flag, p.wait_limit_ns, p.status, 7, peer_abort) ||
+            (kPair && !wait_bounded<true>(bar_peer_full + 8 * stage, phase, abort_flag, p.wait_limit_ns, p.status,
+                                          12, peer_abort))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t sfa_t = tmem + SFA_TMEM0 + stage * SFA_SLOT;
-        const uint32_t sfb_t = tmem + SFB_TMEM0 + stage * SFB_SLOT;
+        const uint32_t sfa_t = tmem + C::SFA_TMEM0 + stage * SFA_SLOT;
+        const uint32_t sfb_t = tmem + C::SFB_TMEM0 + stage * SFB_SLOT;
         // descriptor start addresses advance by 32 bytes (64 FP4 codes) per k-step
         const uint64_t ad = adesc0 + ((stage * A_BYTES) >> 4);
-        const uint64_t bd = bdesc0 + ((stage * B_BYTES) >> 4);
-        if (kb * 4 + 4 <= ksteps) {
+        const uint64_t bd = bdesc0 + ((stage * C::B_BYTES) >> 4);
+        const int nk = kb * 4 + 4 <= ksteps ? 4 : ksteps - kb * 4;
+        if (nk == 4) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            tc_mma_nvf4(tmem, ad + 2 * kk, bd + 2 * kk, idesc, sfa_t + 4 * kk, sfb_t + 8 * kk,
-                        (kb | kk) != 0 ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk) {
+            if constexpr (kPair)
+              tc_mma_nvf4_pair(tmem, ad + 2 * kk, bd + 2 * kk, idesc, sfa_t + 4 * kk, sfb_t + 8 * kk,
+                               (kb | kk) != 0 ? 1u : 0u);
+            else
+              tc_mma_nvf4(tmem, ad + 2 * kk, bd + 2 * kk, idesc, sfa_t + 4 * kk, sfb_t + 8 * kk,
+                          (kb | kk) != 0 ? 1u : 0u);
+          }
         } else {
-          for (int kk = 0; kk < ksteps - kb * 4; ++kk)
-            tc_mma_nvf4(tmem, ad + 2 * kk, bd + 2 * kk, idesc, sfa_t + 4 * kk, sfb_t + 8 * kk,
-                        (kb | kk) != 0 ? 1u : 0u);
+          for (int kk = 0; kk < nk; ++kk) {
+            if constexpr (kPair)
+              tc_mma_nvf4_pair(tmem, ad + 2 * kk, bd + 2 * kk, idesc, sfa_t + 4 * kk, sfb_t + 8 * kk,
+                               (kb | kk) != 0 ? 1u : 0u);
+            else
+              tc_mma_nvf4(tmem, ad + 2 * kk, bd + 2 * kk, idesc, sfa_t + 4 * kk, sfb_t + 8 * kk,
+                          (kb | kk) != 0 ? 1u : 0u);
+          }
         }
         issued = true;
-        tc_commit(bar_empty + 8 * stage);
+        // the stage is free in both CTAs once these MMAs are done
+        if constexpr (kPair) tc_commit_pair_mc(bar_empty + 8 * stage, 0x3);
+        else tc_commit(bar_empty + 8 * stage);
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1;
         }
       }
       if (!ok) break;
-      tc_commit(bar_accf);
+      if constexpr (kPair) tc_commit_pair_mc(bar_accf, 0x3);
+      else tc_commit(bar_accf);
       aphase ^= 1;
     }
     if (!ok && issued) {
       // tensor-core work in flight completes before the tensor memory is freed
-      tc_commit(bar_aux);
+      if constexpr (kPair) tc_commit_pair(bar_aux);
+      else tc_commit(bar_aux);
       drain_wait(bar_aux, 0);
+    }
+  } else if (kPair && warp == 1 && lane == 0) {
+    // ---------------------------------------------------------------- pair relay (odd CTA)
+    // Tells the even CTA's MMA issuer, in the order it consumes them, that this
+    // CTA's stage is loaded and its scales are in tensor memory, and that this
+    // CTA's epilogue has released the accumulator of the previous unit.
+    const uint32_t r_peer_full = mapa_shared(bar_peer_full, 0);
+    const uint32_t r_peer_acce = mapa_shared(bar_peer_acce, 0);
+    uint32_t stage = 0, phase = 0, aph = 0;
+    bool ok = true;
+    for (int i = 0; ok && i < my_units; ++i) {
+      if (i > 0) {
+        if (!wait_bounded(bar_acce, aph, abort_flag, p.wait_limit_ns, p.status, 13, peer_abort)) break;
+        aph ^= 1;
+        mbar_remote_arrive_relaxed(r_peer_acce);
+      }
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!wait_bounded(bar_sfready + 8 * stage, phase, abort_flag, p.wait_limit_ns, p.status, 14, peer_abort) ||
+            !wait_bounded(bar_full + 8 * stage, phase, abort_flag, p.wait_limit_ns, p.status, 15, peer_abort)) {
+          ok = false;
+          break;
+        }
+        mbar_remote_arrive_relaxed(r_peer_full + 8 * stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
     }
   } else if (warp >= kFirstEpiWarp) {
     // ---------------------------------------------------------------- epilogue
@@ -504,10 +632,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = quad * 32 + lane;
     uint32_t aphase = 0;
     const float gs_a = *p.gs_a;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    for (int t = first_unit; t < total; t += unit_stride) {
       int e, nb, mb, rows, ncols;
-      sch.decode(t, e, nb, mb, rows, ncols);
-      if (!wait_bounded(bar_accf, aphase, abort_flag, p.wait_limit_ns, p.status, 4)) break;
+      sch.decode(t, rank, e, nb, mb, rows, ncols);
+      if (!wait_bounded(bar_accf, aphase, abort_flag, p.wait_limit_ns, p.status, 4, peer_abort)) break;
       aphase ^= 1;
       tc_fence_after();
       const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + half * 128;
@@ -603,10 +731,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (kPair) {
+    // neither CTA of the pair leaves (or frees its tensor memory) while the
+    // other may still arrive on its barriers or run MMAs into its tensor memory
+    if (tid == 0) {
+      mbar_remote_arrive(mapa_shared(bar_exit, rank ^ 1));
+      drain_wait<true>(bar_exit, 0);
+    }
+    __syncthreads();
+  }
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, TMEM_COLS);
+    if constexpr (kPair) tmem_dealloc_pair(tmem, TMEM_COLS);
+    else tmem_dealloc(tmem, TMEM_COLS);
   }
 }
 
@@ -648,6 +786,7 @@ bool make_codes_map(CUtensorMap* m, const void* base, int64_t rows, int64_t row_
 int g_num_sms = 0;
 uint64_t g_wait_limit_ns = 4000000000ull;
 int g_test_stall = 0;
+int g_gemm_mode = 0;    // 0: one CTA per tile; 1: 2-SM pairs when N % 256 == 0
 
 int num_sms() {
   if (g_num_sms == 0) {
@@ -659,24 +798,78 @@ int num_sms() {
   return g_num_sms;
 }
 
-size_t smem_bytes(int E) { return (size_t)OFF_SCHED + 8 * (size_t)(E + 1) + 1024; }
+template <bool kPair>
+size_t smem_bytes(int E) { return (size_t)Cfg<kPair>::OFF_SCHED + 8 * (size_t)(E + 1) + 1024; }
+
+// Clusters of two that can be resident at once for a pair kernel (one CTA per
+// SM; a cluster needs two SMs of one GPC), queried once per kernel.
+template <bool kSwiGLU>
+int pair_clusters(size_t smem) {
+  static int cached = -1;
+  if (cached < 0) {
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg<true>::OFF_SCHED + 8 * 1025 + 1024;   // the largest request
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<kSwiGLU, true>, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      n = 0;
+    }
+    cached = n;
+  }
+  (void)smem;
+  return cached;
+}
 
 template <bool kSwiGLU>
 int launch_grouped(const uint8_t* a_codes, int64_t a_rows, const uint8_t* b_codes, int N, int K,
                    Params& p, cudaStream_t s) {
+  // Pairs need whole 256-column weight tiles (each CTA holds 128 of them).
+  const bool pair = g_gemm_mode == 1 && N % BN == 0;
   CUtensorMap ma[4], mb;
   const int boxes[4] = {16, 32, 64, 128};
   for (int i = 0; i < 4; ++i)
     if (!make_codes_map(&ma[i], a_codes, a_rows, K / 2, boxes[i])) return NVFP4MOE_ERR_INVALID;
-  if (!make_codes_map(&mb, b_codes, (int64_t)p.E * N, K / 2, BN)) return NVFP4MOE_ERR_INVALID;
+  if (!make_codes_map(&mb, b_codes, (int64_t)p.E * N, K / 2, pair ? BN / 2 : BN)) return NVFP4MOE_ERR_INVALID;
   int* status = nullptr;
   if (cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_status) != cudaSuccess)
     return NVFP4MOE_ERR_LAUNCH;
   p.status = status;
   p.wait_limit_ns = g_wait_limit_ns;
   p.test_stall = g_test_stall;
-  const size_t smem = smem_bytes(p.E);
-  auto kern = grouped_gemm_kernel<kSwiGLU>;
+  if (pair) {
+    const size_t smem = smem_bytes<true>(p.E);
+    auto kern = grouped_gemm_kernel<kSwiGLU, true>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(Cfg<true>::OFF_SCHED + 8 * 1025 + 1024)) != cudaSuccess)
+      return NVFP4MOE_ERR_LAUNCH;
+    const int clusters = pair_clusters<kSwiGLU>(smem);
+    if (clusters <= 0) return NVFP4MOE_ERR_LAUNCH;
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, ma[0], ma[1], ma[2], ma[3], mb, p) != cudaSuccess) return launch_status();
+    return launch_status();
+  }
+  const size_t smem = smem_bytes<false>(p.E);
+  auto kern = grouped_gemm_kernel<kSwiGLU, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return NVFP4MOE_ERR_LAUNCH;
   const int grid = num_sms();
@@ -782,3 +975,9 @@ extern "C" void nvfp4moe_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns = ns; 
 extern "C" void nvfp4moe_set_test_stall(int on) { g_test_stall = on ? 1 : 0; }
 
 extern "C" int nvfp4moe_num_sms(void) { return num_sms(); }
+
+extern "C" int nvfp4moe_set_gemm_mode(int mode) {
+  if (mode < 0 || mode > 1) return NVFP4MOE_ERR_INVALID;
+  g_gemm_mode = mode;
+  return NVFP4MOE_OK;
+}

@@ -375,3 +375,50 @@ def test_swiglu_epilogue_against_oracle_requant():
     hd_gpu = O.dequantize_f64(gc, gsf, gs_h)
     hd_ref = O.dequantize_f64(hc_ref, hs_ref, gs_h)
     assert cosine(hd_gpu, hd_ref) > 0.9999
+
+
+@pytest.mark.parametrize("swiglu", [False, True])
+def test_pair_kernel_equals_single_cta_kernel(swiglu):
+    """The 2-SM pair kernel (a cluster of two CTAs sharing one tcgen05 MMA of
+    256 rows, each loading half of the weight tile) and the one-CTA-per-tile
+    kernel give the same bits, on groups with odd and even numbers of
+    activation tiles (the odd CTA of a pair then has no rows), an empty group
+    and one-row groups."""
+    rng = np.random.default_rng(31)
+    counts = [1, 0, 129, 256, 300, 77, 512, 1]
+    E, K = len(counts), 1024
+    N = 512 if not swiglu else 1024
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    M = int(offsets[-1])
+    ac, asf, gsa = _rand_q(rng, M, K, 1.0)
+    bl = [_rand_q(rng, N, K, 0.05) for _ in range(E)]
+    a_rows = B.nvfp4moe_padded_rows(M, E)
+    prow = padded_rows_of_compact(offsets)
+    a_pad = np.zeros((a_rows, K // 2), np.uint8)
+    a_pad[prow] = ac
+    asf_rm = np.zeros((a_rows, K // 16), np.uint8)
+    asf_rm[prow] = asf
+    d = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(DEV)
+    args = (d(a_pad), d(_rows_sf(asf_rm, a_rows, K)), d(np.array([gsa], np.float32)),
+            d(np.stack([b[0] for b in bl])), d(np.concatenate([_tile_sf(b[1], N, K) for b in bl])),
+            d(np.array([b[2] for b in bl], np.float32)), d(offsets))
+    outs = []
+    for mode in (1, 0):
+        B.nvfp4moe_set_gemm_mode(mode)
+        try:
+            if swiglu:
+                hc, hs = B.nvfp4_grouped_gemm_swiglu(*args, d(np.array([2688.0 / 4.0], np.float32)))
+                outs.append((hc.cpu()[torch.from_numpy(prow)], hs.cpu()[torch.from_numpy(sf_rows_index(a_rows, N // 2)[prow].reshape(-1))]))
+            else:
+                outs.append((B.nvfp4_grouped_gemm(*args).cpu(),))
+        finally:
+            B.nvfp4moe_set_gemm_mode(0)
+        assert B.nvfp4moe_last_device_status() == 0
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
+    if not swiglu:
+        ref = O.grouped_gemm(ac, asf, gsa, np.stack([b[0] for b in bl]), np.stack([b[1] for b in bl]),
+                             np.array([b[2] for b in bl], np.float32), offsets)
+        got = outs[0][0].float().numpy()
+        assert_close_tol(got, ref, "pair")
+        assert cosine(got, ref) > 0.9999

@@ -30,24 +30,32 @@ def _operands():
     return a_codes, a_sf, one, b_codes, b_sf, gsb, offsets
 
 
-def test_wait_timeout_is_reported_and_context_survives():
+@pytest.mark.parametrize("mode", [0, 1])
+def test_wait_timeout_is_reported_and_context_survives(mode):
+    """mode 0: one CTA per tile; mode 1: the 2-SM pair kernel (the even CTA's
+    MMA issuer stalls; the odd CTA learns of the abort from its flag, which the
+    even CTA sets remotely, and both leave through the exit handshake)."""
     ops = _operands()
-    assert B.nvfp4moe_last_device_status() == 0
-    good = B.nvfp4_grouped_gemm(*ops).clone()
-    assert B.nvfp4moe_last_device_status() == 0
+    B.nvfp4moe_set_gemm_mode(mode)
     try:
-        B.nvfp4moe_set_wait_limit_ns(20_000_000)      # 20 ms
-        B.nvfp4moe_set_test_stall(True)
-        B.nvfp4_grouped_gemm(*ops)
-        st = B.nvfp4moe_last_device_status()
+        assert B.nvfp4moe_last_device_status() == 0
+        good = B.nvfp4_grouped_gemm(*ops).clone()
+        assert B.nvfp4moe_last_device_status() == 0
+        try:
+            B.nvfp4moe_set_wait_limit_ns(20_000_000)      # 20 ms
+            B.nvfp4moe_set_test_stall(True)
+            B.nvfp4_grouped_gemm(*ops)
+            st = B.nvfp4moe_last_device_status()
+        finally:
+            B.nvfp4moe_set_test_stall(False)
+            B.nvfp4moe_set_wait_limit_ns(4_000_000_000)
+        assert st == -5
+        # status was read and cleared; a normal launch still works and matches
+        again = B.nvfp4_grouped_gemm(*ops)
+        assert B.nvfp4moe_last_device_status() == 0
+        assert torch.equal(good, again)
     finally:
-        B.nvfp4moe_set_test_stall(False)
-        B.nvfp4moe_set_wait_limit_ns(4_000_000_000)
-    assert st == -5
-    # status was read and cleared; a normal launch still works and matches
-    again = B.nvfp4_grouped_gemm(*ops)
-    assert B.nvfp4moe_last_device_status() == 0
-    assert torch.equal(good, again)
+        B.nvfp4moe_set_gemm_mode(0)
     assert torch.isfinite(good.float()).all()
 
 

@@ -14,30 +14,42 @@
 // (about 35 bytes of TMEM per cycle, one copy engine) costs more than the MMAs
 // it feeds, so four warps write them with tcgen05.st instead, each into its
 // own TMEM lane quadrant, in parallel.
-// Warp roles (448 threads, one CTA per SM):
+// Warp roles (480 threads, one CTA per SM):
 //   warp 0      TMA producer: A and B code tiles (tiled TMA, 128B swizzle)
 //               into a 4-stage ring
 //   warp 1      TMEM owner; one lane issues the MMAs
-//   warps 2-5   scale warps, one per TMEM lane quadrant q. A stage's scales
-//               (activation: 128 rows x 16 bytes, row-tiled layout; weights:
-//               512-byte atoms) reach a shared-memory ring either by the
-//               producer's bulk copies (L1) or by the scale warps' own
-//               cp.async copies up to 4 stages ahead (L2: the load path adds
-//               to the TMA engine's bandwidth, which the code tiles
-//               saturate). Per K=64 step the A scale of each of the quadrant's
-//               32 rows goes to column 4kk+q (the MMA reads quadrant q's A
-//               scales from column base+q), and the 256 B-row scales to
-//               columns 8kk..8kk+7 (B scales are read in every quadrant, so
-//               each quadrant holds its own copy)
+//   warps 2-5   scale warps, one per TMEM lane quadrant q: per stage, once the
+//               stage's scale atoms have landed, the A scale of each of the
+//               quadrant's 32 rows goes to column 4kk+q for K=64 step kk (the
+//               MMA reads quadrant q's A scales from column base+q), and the
+//               256 B-row scales to columns 8kk..8kk+7 (B scales are read in
+//               every quadrant, so each quadrant holds its own copy)
 //   warps 6-13  epilogue, two warps per TMEM lane quadrant (128 columns
 //               each): the f32 accumulator is moved to registers and released
 //               (L1: the first 64 columns become h before the second 64 are
 //               loaded), so the next tile's MMAs overlap the epilogue math;
 //               then BF16 output (L2, streaming stores) or SwiGLU + NVFP4
 //               requant (L1, h in the row-tiled scale layout the L2 GEMM reads)
+//   warp 14     one lane issues the scale atoms' bulk copies (activation:
+//               128 rows x 16 bytes, row-tiled layout; weights: 512-byte
+//               atoms) of each stage into its scale slot, after the same wait
+//               for a free stage as the producer. Per stage the load round trip
+//               (slot free -> copies issued -> landed -> MMAs -> slot free)
+//               bounds the kernel, and issuing five copies from one thread put
+//               ~640 cycles of it on every stage; with the scale copies here
+//               the producer spends ~160.
 // Tiles are ordered expert-major, then weight tile, then activation tile, so
 // the activation tiles sharing one weight tile run at the same time on
 // neighbouring SMs and the weight tile leaves HBM once.
+//
+// 2-SM pairs (kPair, opt-in): a cluster of two CTAs on one tile of 256
+// activation rows (the even CTA's 128, then the odd CTA's) x 256 weight rows;
+// each CTA loads its activation rows and half of the weight rows, and the even
+// CTA issues tcgen05.mma.cta_group::2 (M=256) whose result rows land in each
+// CTA's own tensor memory. The odd CTA's relay thread tells the even CTA's MMA
+// issuer when its stage is loaded and its scales stored, and when its
+// epilogue has released the accumulator; the MMA commits arrive on both CTAs'
+// barriers.
 //
 // Every wait is bounded: a wait that exceeds the limit sets the device status
 // word, raises a shared abort flag that ends the other roles' loops, and the
@@ -57,11 +69,11 @@ constexpr int BK = 256;                       // K elements per stage
 constexpr int kScaleWarps = 4;
 constexpr int kEpiWarps = 8;
 constexpr int kFirstEpiWarp = 2 + kScaleWarps;
-constexpr int kThreads = 32 * (2 + kScaleWarps + kEpiWarps);
+constexpr int kCopyWarp = kFirstEpiWarp + kEpiWarps;   // issues the scale atoms' bulk copies
+constexpr int kThreads = 32 * (kCopyWarp + 1);
 constexpr int A_BYTES = BM * BK / 2;          // 16 KB
 constexpr int SFA_BYTES = 4 * 512;            // 4 scale atoms (K=256) of 128 rows
 constexpr int SF_BYTES = 3 * SFA_BYTES;       // SFA, then SFB's two 128-row halves
-constexpr int kScaleThreads = 32 * 4;         // the scale warps
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COLS = BN;             // one f32 accumulator of 256 columns
 constexpr uint32_t SFB_SLOT = 32;
@@ -89,7 +101,7 @@ struct Cfg {
   static constexpr uint32_t SFA_TMEM0 = SFB_TMEM0 + STAGES * SFB_SLOT;
   static_assert(SFA_TMEM0 + STAGES * SFA_SLOT <= TMEM_COLS, "tensor memory budget");
   static_assert(OFF_SCHED + 8 * 1025 + 1024 <= 232448, "shared memory budget");
-  static_assert((kPair ? 7 * STAGES + 6 : 6 * STAGES + 4) * 8 <= OFF_MISC - OFF_BAR, "barrier area");
+  static_assert((kPair ? 5 * STAGES + 7 : 4 * STAGES + 4) * 8 <= OFF_MISC - OFF_BAR, "barrier area");
 };
 
 struct Params {
@@ -209,20 +221,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_acce = bar_accf + 8;
   const uint32_t bar_aux = bar_acce + 8;                   // MMA drain on abort
   const uint32_t bar_never = bar_aux + 8;                  // never arrived on (failure-path test)
-  const uint32_t bar_sfland = bar_never + 8;               // STAGES: a stage's scale atoms landed
-  const uint32_t bar_sfcons = bar_sfland + STAGES * 8;     // STAGES: its scale atoms read by all scale warps
-  const uint32_t bar_sffull = bar_sfcons + STAGES * 8;     // STAGES: scale atoms copied by the producer landed
+  const uint32_t bar_sffull = bar_never + 8;               // STAGES: a stage's scale atoms landed
   // pairs: the odd CTA's stage s is loaded and its scales stored (arrived on
   // from the odd CTA, used by the even CTA's MMA issuer); the odd CTA's
   // epilogue released the accumulator; the exit handshake
   const uint32_t bar_peer_full = bar_sffull + STAGES * 8;  // STAGES
   const uint32_t bar_peer_acce = bar_peer_full + STAGES * 8;
   const uint32_t bar_exit = bar_peer_acce + 8;
-  // Scale atoms reach shared memory either as bulk copies from the TMA
-  // producer (L1: its epilogue's register spills use the load path) or as
-  // cp.async copies from the scale warps (L2), whose load path adds to the
-  // TMA engine's bandwidth.
-  constexpr bool kScalesByTMA = kSwiGLU;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   int32_t* tile_start = reinterpret_cast<int32_t*>(smem + C::OFF_SCHED);
@@ -268,8 +273,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_sfready + 8 * s, kScaleWarps);
-      mbar_init(bar_sfland + 8 * s, kScaleThreads);
-      mbar_init(bar_sfcons + 8 * s, kScaleWarps);
       mbar_init(bar_sffull + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
       if constexpr (kPair) mbar_init(bar_peer_full + 8 * s, 1);
@@ -319,13 +322,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t pol_w1 = l2_policy_evict_first();
     const uint64_t pol_wn = l2_policy_evict_normal();
     const uint64_t pol_a = l2_policy_evict_last();   // activations: reused by every weight tile
-    // Copy sources of one unit, decoded one unit ahead of its loads.
+    // Copy sources of one unit's code tiles, decoded one unit ahead of its loads.
     struct TileSrc {
       const CUtensorMap* tma;
-      int box, a_row, b_row, bhalves;
+      int box, a_row, b_row;
       bool has_a;
-      const uint8_t* sfa;
-      const uint8_t* sfb;
       uint64_t pol_w;
     };
     auto tile_src = [&](int t) {
@@ -338,9 +339,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       c.box = rows <= 16 ? 16 : rows <= 32 ? 32 : rows <= 64 ? 64 : 128;
       c.a_row = pad_off[e] + mb * BM;
       c.b_row = e * p.N + nb * BN + rank * C::B_ROWS;
-      c.bhalves = ncols / 128;
-      c.sfa = p.a_sf + (int64_t)(c.a_row / BM) * p.a_sf_rowtile_bytes;
-      c.sfb = p.b_sf + (int64_t)e * p.b_sf_expert_bytes + (int64_t)(nb * 2) * p.sf_rowtile_bytes;
       return c;
     };
     uint32_t stage = 0, phase = 0, filled = 0, fill_phase = 0;
@@ -354,17 +352,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_bounded(bar_empty + 8 * stage, phase ^ 1, abort_flag, p.wait_limit_ns, p.status, 1, peer_abort)) {
           ok = false;
           break;
-        }
-        if constexpr (kScalesByTMA) {
-          const int nk = min(4, ksteps - kb * 4);
-          const uint32_t sffull = bar_sffull + 8 * stage;
-          const uint32_t sdst = sbase + C::OFF_SF + stage * SF_BYTES;
-          // the activation scales of a stage are 2048 bytes whatever the K tail
-          mbar_arrive_expect_tx(sffull, (cur.has_a ? 2048 : 0) + cur.bhalves * nk * 512);
-          if (cur.has_a) bulk_load(sdst, cur.sfa + kb * 2048, 2048, sffull, pol_a);
-          for (int h = 0; h < cur.bhalves; ++h)
-            bulk_load(sdst + SFA_BYTES + h * SFA_BYTES, cur.sfb + h * p.sf_rowtile_bytes + kb * 2048, nk * 512,
-                      sffull, cur.pol_w);
         }
         const uint32_t full = bar_full + 8 * stage;
         // the B box always moves B_ROWS rows; rows past this expert's last
@@ -385,10 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok) {
       // copies still in flight complete before the CTA may exit
       for (int s = 0; s < STAGES; ++s)
-        if ((filled >> s) & 1u) {
-          drain_wait(bar_full + 8 * s, (fill_phase >> s) & 1u);
-          if constexpr (kScalesByTMA) drain_wait(bar_sffull + 8 * s, (fill_phase >> s) & 1u);
-        }
+        if ((filled >> s) & 1u) drain_wait(bar_full + 8 * s, (fill_phase >> s) & 1u);
     } else if constexpr (kPair) {
       // every stage's last use released by the even CTA's MMAs (whose commits
       // arrive on this CTA's barriers) before the CTA may exit
@@ -401,65 +385,63 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp >= 2 && warp < kFirstEpiWarp) {
-    // ---------------------------------------------------------------- scale warps
-    // The scale atoms travel through the load path (cp.async), not the TMA
-    // engine that the code tiles saturate: the 128 scale threads copy a stage's
-    // atoms (up to 6 KB) into a STAGES-slot shared-memory ring up to STAGES
-    // stages ahead; a slot is refilled once all four warps have read it. Per
-    // stage, each warp then stores its quadrant's scales into the stage's TMEM
-    // slot. A pair CTA without an activation tile in the unit stores zero A
-    // scales (its rows of the MMA are discarded).
-    const int q = warp & 3;                               // TMEM lane quadrant of this warp
-    const uint32_t lanes = static_cast<uint32_t>(q * 32) << 16;
-    const int st_id = (warp - 2) * 32 + lane;              // 0..127 among the scale threads
-    const int nstages = my_units * kblocks;
-    // copy cursor: unit, k-block and the unit's scale sources
-    int ct = first_unit, ckb = 0;
-    const uint8_t* csfa = nullptr;
-    const uint8_t* csfb = nullptr;
-    bool ctwo = false, chas_a = true;
-    auto load_tile = [&](int t) {
+  } else if (warp == kCopyWarp && lane == 0) {
+    // ---------------------------------------------------------------- scale copies
+    // The scale atoms of each stage (activation: 128 rows x 16 bytes, 2048
+    // bytes whatever the K tail; weights: the 512-byte atoms of the tile's two
+    // 128-row halves) as bulk copies into the stage's scale slot, once the
+    // stage is free (the same wait as the producer's). A thread of its own, so
+    // that the producer issues only the two code tiles per stage: each copy
+    // costs its issuing thread ~130 cycles, and with all five on one thread
+    // that issue time sat on the load round trip of every stage.
+    const uint64_t pol_a = l2_policy_evict_last();
+    const uint64_t pol_w1 = l2_policy_evict_first();
+    const uint64_t pol_wn = l2_policy_evict_normal();
+    uint32_t stage = 0, phase = 0, filled = 0, fill_phase = 0;
+    bool ok = true;
+    for (int t = first_unit; ok && t < total; t += unit_stride) {
       int e, nb, mb, rows, ncols;
       sch.decode(t, rank, e, nb, mb, rows, ncols);
-      csfa = p.a_sf + (int64_t)((pad_off[e] + mb * BM) / BM) * p.a_sf_rowtile_bytes;
-      csfb = p.b_sf + (int64_t)e * p.b_sf_expert_bytes + (int64_t)(nb * 2) * p.sf_rowtile_bytes;
-      ctwo = ncols > 128;
-      chas_a = rows > 0;
-    };
-    if (!kScalesByTMA && nstages > 0) load_tile(ct);
-    bool ok = true;
-    int gc = 0;                                           // next stage to copy
-    auto issue = [&]() -> bool {
-      if constexpr (kScalesByTMA) return true;           // the producer copies the atoms
-      const int slot = gc % STAGES, use = gc / STAGES;
-      if (use > 0 &&
-          !wait_bounded(bar_sfcons + 8 * slot, (use - 1) & 1, abort_flag, p.wait_limit_ns, p.status, 5, peer_abort))
-        return false;
-      const int nk = min(4, ksteps - ckb * 4);
-      const uint32_t dst = sbase + C::OFF_SF + slot * SF_BYTES;
-      // 384 chunks of 16 bytes: the activation scales (128 rows x 16 bytes),
-      // then the weight scale atoms of halves 0 and 1 (128 each); weight atoms
-      // past a K tail, or of a missing second half, are not copied
-#pragma unroll
-      for (int i = 0; i < 3; ++i) {
-        const int c = st_id + kScaleThreads * i;           // region i, chunk st_id
-        const bool live = i == 0 ? chas_a : (st_id < nk * 32 && (i < 2 || ctwo));
-        if (live) {
-          const uint8_t* src = i == 0 ? csfa + ckb * 2048 + st_id * 16
-                                      : csfb + (int64_t)(i - 1) * p.sf_rowtile_bytes + ckb * 2048 + st_id * 16;
-          cp_async_16(dst + c * 16, src);
+      const bool has_a = rows > 0;
+      const uint64_t pol_w = tile_start[e + 1] - tile_start[e] > NT ? pol_wn : pol_w1;
+      const uint8_t* sfa = p.a_sf + (int64_t)((pad_off[e] + mb * BM) / BM) * p.a_sf_rowtile_bytes;
+      const uint8_t* sfb = p.b_sf + (int64_t)e * p.b_sf_expert_bytes + (int64_t)(nb * 2) * p.sf_rowtile_bytes;
+      const int bhalves = ncols / 128;
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!wait_bounded(bar_empty + 8 * stage, phase ^ 1, abort_flag, p.wait_limit_ns, p.status, 16, peer_abort)) {
+          ok = false;
+          break;
+        }
+        const int nk = min(4, ksteps - kb * 4);
+        const uint32_t sffull = bar_sffull + 8 * stage;
+        const uint32_t sdst = sbase + C::OFF_SF + stage * SF_BYTES;
+        mbar_arrive_expect_tx(sffull, (has_a ? 2048 : 0) + bhalves * nk * 512);
+        if (has_a) bulk_load(sdst, sfa + kb * 2048, 2048, sffull, pol_a);
+        for (int h = 0; h < bhalves; ++h)
+          bulk_load(sdst + SFA_BYTES + h * SFA_BYTES, sfb + h * p.sf_rowtile_bytes + kb * 2048, nk * 512, sffull,
+                    pol_w);
+        filled |= 1u << stage;
+        fill_phase = (fill_phase & ~(1u << stage)) | (phase << stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
         }
       }
-      cp_async_arrive_noinc(bar_sfland + 8 * slot);
-      ++gc;
-      if (++ckb == kblocks) {
-        ckb = 0;
-        ct += unit_stride;
-        if (ct < total) load_tile(ct);
-      }
-      return true;
-    };
+    }
+    if (!ok)   // copies still in flight complete before the CTA may exit
+      for (int s = 0; s < STAGES; ++s)
+        if ((filled >> s) & 1u) drain_wait(bar_sffull + 8 * s, (fill_phase >> s) & 1u);
+  } else if (warp >= 2 && warp < kFirstEpiWarp) {
+    // ---------------------------------------------------------------- scale warps
+    // Per stage, each warp stores its quadrant's scales into the stage's TMEM
+    // slot once the stage's atoms have landed (the slot's previous MMAs are
+    // done by then: the copies were issued after them). A pair CTA without an
+    // activation tile in the unit stores zero A scales (its rows of the MMA
+    // are discarded).
+    const int q = warp & 3;                               // TMEM lane quadrant of this warp
+    const uint32_t lanes = static_cast<uint32_t>(q * 32) << 16;
+    const int nstages = my_units * kblocks;
+    bool ok = true;
     bool use_has_a = true;                                // the consumed unit has this CTA's activation tile
     for (int g = 0; ok && g < nstages; ++g) {
       if constexpr (kPair) {
@@ -469,13 +451,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           use_has_a = rows > 0;
         }
       }
-      if constexpr (!kScalesByTMA) {
-        while (ok && gc < nstages && gc < g + STAGES) ok = __all_sync(0xFFFFFFFFu, issue());
-        if (!ok) break;
-      }
       const int slot = g % STAGES, use = g / STAGES;
-      ok = wait_bounded((kScalesByTMA ? bar_sffull : bar_sfland) + 8 * slot, use & 1, abort_flag,
-                        p.wait_limit_ns, p.status, 5, peer_abort);
+      ok = wait_bounded(bar_sffull + 8 * slot, use & 1, abort_flag, p.wait_limit_ns, p.status, 5, peer_abort);
       ok = __all_sync(0xFFFFFFFFu, ok);
       if (!ok) break;
       // Activation scales: row r's 16 blocks are the 16 bytes at r * 16, the
@@ -496,14 +473,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         b[8 * kk + 4] = hi.x; b[8 * kk + 5] = hi.y; b[8 * kk + 6] = hi.z; b[8 * kk + 7] = hi.w;
       }
       __syncwarp();
-      if constexpr (!kScalesByTMA) {
-        if (lane == 0) mbar_arrive(bar_sfcons + 8 * slot);
-        // the TMEM slot is free once the MMAs of its previous use completed
-        // (with producer copies, their landing already implies it)
-        ok = wait_bounded(bar_empty + 8 * slot, (use & 1) ^ 1, abort_flag, p.wait_limit_ns, p.status, 5, peer_abort);
-        ok = __all_sync(0xFFFFFFFFu, ok);
-        if (!ok) break;
-      }
       const uint32_t sfa_t = tmem + lanes + C::SFA_TMEM0 + slot * SFA_SLOT + q;
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) tc_st1(sfa_t + 4 * kk, a[kk]);
@@ -513,8 +482,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_sfready + 8 * slot);
     }
-    // this thread's copies land before the CTA may exit
-    cp_async_wait_all();
   } else if (warp == 1 && lane == 0 && rank == 0) {
     // ---------------------------------------------------------------- MMA issuer
     uint32_t stage = 0, phase = 0, aphase = 0;
@@ -625,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp >= kFirstEpiWarp) {
+  } else if (warp >= kFirstEpiWarp && warp < kFirstEpiWarp + kEpiWarps) {
     // ---------------------------------------------------------------- epilogue
     const int quad = warp & 3;                 // TMEM lane quadrant this warp may access
     const int half = (warp - kFirstEpiWarp) >> 2;   // columns [128*half, 128*half + 128)

@@ -101,7 +101,7 @@ struct Cfg {
   static constexpr uint32_t SFA_TMEM0 = SFB_TMEM0 + STAGES * SFB_SLOT;
   static_assert(SFA_TMEM0 + STAGES * SFA_SLOT <= TMEM_COLS, "tensor memory budget");
   static_assert(OFF_SCHED + 8 * 1025 + 1024 <= 232448, "shared memory budget");
-  static_assert((kPair ? 5 * STAGES + 7 : 4 * STAGES + 4) * 8 <= OFF_MISC - OFF_BAR, "barrier area");
+  static_assert((kPair ? 4 * STAGES + 7 : 3 * STAGES + 4) * 8 <= OFF_MISC - OFF_BAR, "barrier area");
 };
 
 struct Params {
@@ -214,9 +214,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t sbase = smem_addr(smem);
+  // full[s]: stage s's code tiles landed (the producer's expect_tx) and its
+  // scales are in tensor memory (one arrival per scale warp): the one barrier
+  // the MMA issuer waits on per stage (every wait in its loop costs the tensor
+  // pipe; measured, the per-stage waits were ~11% of a load-free MMA stream)
   const uint32_t bar_full = sbase + C::OFF_BAR;            // STAGES x 8 bytes each
-  const uint32_t bar_sfready = bar_full + STAGES * 8;
-  const uint32_t bar_empty = bar_sfready + STAGES * 8;
+  const uint32_t bar_empty = bar_full + STAGES * 8;
   const uint32_t bar_accf = bar_empty + STAGES * 8;
   const uint32_t bar_acce = bar_accf + 8;
   const uint32_t bar_aux = bar_acce + 8;                   // MMA drain on abort
@@ -271,8 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (tid == 32) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_sfready + 8 * s, kScaleWarps);
+      mbar_init(bar_full + 8 * s, 1 + kScaleWarps);
       mbar_init(bar_sffull + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
       if constexpr (kPair) mbar_init(bar_peer_full + 8 * s, 1);
@@ -443,7 +445,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nstages = my_units * kblocks;
     bool ok = true;
     bool use_has_a = true;                                // the consumed unit has this CTA's activation tile
-    for (int g = 0; ok && g < nstages; ++g) {
+    int g = 0;
+    for (; ok && g < nstages; ++g) {
       if constexpr (kPair) {
         if (g % kblocks == 0) {
           int e, nb, mb, rows, ncols;
@@ -480,8 +483,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_sfready + 8 * slot);
+      if (lane == 0) mbar_arrive(bar_full + 8 * slot);
     }
+    // After an abort the stages this warp did not process still get its
+    // arrival, so that the producer's drain of its copies in flight (a wait on
+    // the same barriers) completes as soon as they land.
+    if (!ok && lane == 0)
+      for (int i = 0; i < STAGES && g + i < nstages; ++i) mbar_arrive(bar_full + 8 * ((g + i) % STAGES));
   } else if (warp == 1 && lane == 0 && rank == 0) {
     // ---------------------------------------------------------------- MMA issuer
     uint32_t stage = 0, phase = 0, aphase = 0;
@@ -510,8 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       for (int kb = 0; kb < kblocks; ++kb) {
-        if (!wait_bounded(bar_sfready + 8 * stage, phase, abort_flag, p.wait_limit_ns, p.status, 3, peer_abort) ||
-            !wait_bounded(bar_full + 8 * stage, phase, abort_flag, p.wait_limit_ns, p.status, 7, peer_abort) ||
+        if (!wait_bounded(bar_full + 8 * stage, phase, abort_flag, p.wait_limit_ns, p.status, 7, peer_abort) ||
             (kPair && !wait_bounded<true>(bar_peer_full + 8 * stage, phase, abort_flag, p.wait_limit_ns, p.status,
                                           12, peer_abort))) {
           ok = false;
@@ -580,8 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_remote_arrive_relaxed(r_peer_acce);
       }
       for (int kb = 0; kb < kblocks; ++kb) {
-        if (!wait_bounded(bar_sfready + 8 * stage, phase, abort_flag, p.wait_limit_ns, p.status, 14, peer_abort) ||
-            !wait_bounded(bar_full + 8 * stage, phase, abort_flag, p.wait_limit_ns, p.status, 15, peer_abort)) {
+        if (!wait_bounded(bar_full + 8 * stage, phase, abort_flag, p.wait_limit_ns, p.status, 15, peer_abort)) {
           ok = false;
           break;
         }

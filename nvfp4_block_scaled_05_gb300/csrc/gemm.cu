@@ -46,9 +46,10 @@
 // activation rows (the even CTA's 128, then the odd CTA's) x 256 weight rows;
 // each CTA loads its activation rows and half of the weight rows, and the even
 // CTA issues tcgen05.mma.cta_group::2 (M=256) whose result rows land in each
-// CTA's own tensor memory. The odd CTA's relay thread tells the even CTA's MMA
-// issuer when its stage is loaded and its scales stored, and when its
-// epilogue has released the accumulator; the MMA commits arrive on both CTAs'
+// CTA's own tensor memory. Both CTAs' code tiles complete on the even CTA's
+// stage barrier (the pair form of the tensor copy), both CTAs' scale warps and
+// epilogues arrive on the even CTA's barriers, so the MMA issuer waits once
+// per stage as in the one-CTA kernel; the MMA commits arrive on both CTAs'
 // barriers.
 //
 // Every wait is bounded: a wait that exceeds the limit sets the device status
@@ -79,6 +80,7 @@ constexpr uint32_t ACC_COLS = BN;             // one f32 accumulator of 256 colu
 constexpr uint32_t SFB_SLOT = 32;
 constexpr uint32_t SFA_SLOT = 16;
 constexpr uint64_t kDrainLimitNs = 1000000000ull;
+constexpr uint64_t kPairCopyDrainNs = 2000000ull;   // 2 ms
 
 // Shared- and tensor-memory plan of one CTA. kPair: the CTA is one half of a
 // 2-SM pair and holds only its 128 of the tile's 256 weight rows, which frees
@@ -101,7 +103,7 @@ struct Cfg {
   static constexpr uint32_t SFA_TMEM0 = SFB_TMEM0 + STAGES * SFB_SLOT;
   static_assert(SFA_TMEM0 + STAGES * SFA_SLOT <= TMEM_COLS, "tensor memory budget");
   static_assert(OFF_SCHED + 8 * 1025 + 1024 <= 232448, "shared memory budget");
-  static_assert((kPair ? 4 * STAGES + 7 : 3 * STAGES + 4) * 8 <= OFF_MISC - OFF_BAR, "barrier area");
+  static_assert((kPair ? 3 * STAGES + 5 : 3 * STAGES + 4) * 8 <= OFF_MISC - OFF_BAR, "barrier area");
 };
 
 struct Params {
@@ -225,12 +227,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_aux = bar_acce + 8;                   // MMA drain on abort
   const uint32_t bar_never = bar_aux + 8;                  // never arrived on (failure-path test)
   const uint32_t bar_sffull = bar_never + 8;               // STAGES: a stage's scale atoms landed
-  // pairs: the odd CTA's stage s is loaded and its scales stored (arrived on
-  // from the odd CTA, used by the even CTA's MMA issuer); the odd CTA's
-  // epilogue released the accumulator; the exit handshake
-  const uint32_t bar_peer_full = bar_sffull + STAGES * 8;  // STAGES
-  const uint32_t bar_peer_acce = bar_peer_full + STAGES * 8;
-  const uint32_t bar_exit = bar_peer_acce + 8;
+  // pairs: the exit handshake
+  const uint32_t bar_exit = bar_sffull + STAGES * 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   int32_t* tile_start = reinterpret_cast<int32_t*>(smem + C::OFF_SCHED);
@@ -241,6 +239,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int first_unit = kPair ? (int)blockIdx.x / 2 : (int)blockIdx.x;
   const int unit_stride = kPair ? (int)gridDim.x / 2 : (int)gridDim.x;
   const uint32_t peer_abort = kPair ? mapa_shared(smem_addr(smem + C::OFF_MISC + 4), rank ^ 1) : 0u;
+  // pairs: the even CTA's full barriers (both CTAs' code tiles complete on
+  // them and both CTAs' scale warps arrive on them) and accumulator-empty
+  // barrier (both CTAs' epilogues arrive on it), as shared::cluster addresses
+  const uint32_t pair_full0 = kPair ? mapa_shared(bar_full, 0) : 0u;
+  const uint32_t pair_acce = kPair ? mapa_shared(bar_acce, 0) : 0u;
 
   // --- schedule: per expert its units (ceil(n_e/128) activation tiles, or
   //     ceil of half of that with pairs, per weight tile), prefix sums
@@ -274,19 +277,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (tid == 32) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(bar_full + 8 * s, 1 + kScaleWarps);
+      // pairs (used in the even CTA only): the even producer's expect_tx and
+      // the scale warps of both CTAs
+      mbar_init(bar_full + 8 * s, 1 + kScaleWarps * (kPair ? 2 : 1));
       mbar_init(bar_sffull + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
-      if constexpr (kPair) mbar_init(bar_peer_full + 8 * s, 1);
     }
     mbar_init(bar_accf, 1);
-    mbar_init(bar_acce, kEpiWarps * 32);
+    // every epilogue thread of this CTA; pairs: and one lane per epilogue warp
+    // of the odd CTA
+    mbar_init(bar_acce, kEpiWarps * 32 + (kPair ? kEpiWarps : 0));
     mbar_init(bar_aux, 1);
     mbar_init(bar_never, 1);
-    if constexpr (kPair) {
-      mbar_init(bar_peer_acce, 1);
-      mbar_init(bar_exit, 1);
-    }
+    if constexpr (kPair) mbar_init(bar_exit, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -325,12 +328,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t pol_wn = l2_policy_evict_normal();
     const uint64_t pol_a = l2_policy_evict_last();   // activations: reused by every weight tile
     // Copy sources of one unit's code tiles, decoded one unit ahead of its loads.
+    // pairs: tx_bytes also counts the odd CTA's tiles (the even CTA arms the
+    // barrier both CTAs' copies complete on)
     struct TileSrc {
       const CUtensorMap* tma;
       int box, a_row, b_row;
+      uint32_t tx_bytes;
       bool has_a;
       uint64_t pol_w;
     };
+    auto a_box = [](int rows) { return rows <= 0 ? 0 : rows <= 16 ? 16 : rows <= 32 ? 32 : rows <= 64 ? 64 : 128; };
     auto tile_src = [&](int t) {
       int e, nb, mb, rows, ncols;
       sch.decode(t, rank, e, nb, mb, rows, ncols);
@@ -338,9 +345,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       c.pol_w = tile_start[e + 1] - tile_start[e] > NT ? pol_wn : pol_w1;
       c.has_a = rows > 0;
       c.tma = rows <= 16 ? &tm_a16 : rows <= 32 ? &tm_a32 : rows <= 64 ? &tm_a64 : &tm_a128;
-      c.box = rows <= 16 ? 16 : rows <= 32 ? 32 : rows <= 64 ? 64 : 128;
+      c.box = a_box(rows);
       c.a_row = pad_off[e] + mb * BM;
       c.b_row = e * p.N + nb * BN + rank * C::B_ROWS;
+      c.tx_bytes = (uint32_t)(c.box * 128 + C::B_ROWS * 128);
+      if constexpr (kPair) {
+        if (rank == 0) {
+          int e1, nb1, mb1, rows1, ncols1;
+          sch.decode(t, 1, e1, nb1, mb1, rows1, ncols1);
+          c.tx_bytes += (uint32_t)(a_box(rows1) * 128 + C::B_ROWS * 128);
+        }
+      }
       return c;
     };
     uint32_t stage = 0, phase = 0, filled = 0, fill_phase = 0;
@@ -355,13 +370,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        const uint32_t full = bar_full + 8 * stage;
         // the B box always moves B_ROWS rows; rows past this expert's last
         // weight tile are never multiplied (N=128 MMA), rows past the tensor
         // read zeros
-        mbar_arrive_expect_tx(full, (cur.has_a ? cur.box * 128 : 0) + C::B_ROWS * 128);
-        if (cur.has_a) tma_load_2d(sbase + stage * A_BYTES, cur.tma, full, kb * 128, cur.a_row, pol_a);
-        tma_load_2d(sbase + C::OFF_B + stage * C::B_BYTES, &tm_b, full, kb * 128, cur.b_row, cur.pol_w);
+        if constexpr (kPair) {
+          // both CTAs' tiles complete on the even CTA's barrier, which only
+          // the even CTA arms (a copy may land before it is armed: the phase
+          // cannot complete while the arrival is missing)
+          const uint32_t full = pair_full0 + 8 * stage;
+          if (rank == 0) mbar_arrive_expect_tx(bar_full + 8 * stage, cur.tx_bytes);
+          if (cur.has_a) tma_load_2d_pair(sbase + stage * A_BYTES, cur.tma, full, kb * 128, cur.a_row, pol_a);
+          tma_load_2d_pair(sbase + C::OFF_B + stage * C::B_BYTES, &tm_b, full, kb * 128, cur.b_row, cur.pol_w);
+        } else {
+          const uint32_t full = bar_full + 8 * stage;
+          mbar_arrive_expect_tx(full, cur.tx_bytes);
+          if (cur.has_a) tma_load_2d(sbase + stage * A_BYTES, cur.tma, full, kb * 128, cur.a_row, pol_a);
+          tma_load_2d(sbase + C::OFF_B + stage * C::B_BYTES, &tm_b, full, kb * 128, cur.b_row, cur.pol_w);
+        }
         filled |= 1u << stage;
         fill_phase = (fill_phase & ~(1u << stage)) | (phase << stage);
         if (++stage == STAGES) {
@@ -372,9 +397,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       cur = nxt;
     }
     if (!ok) {
-      // copies still in flight complete before the CTA may exit
-      for (int s = 0; s < STAGES; ++s)
-        if ((filled >> s) & 1u) drain_wait(bar_full + 8 * s, (fill_phase >> s) & 1u);
+      // copies still in flight complete before the CTA may exit. A pair's
+      // copies complete on the even CTA's barriers together with the other
+      // CTA's, whose producer may have stopped before arming or issuing its
+      // part, so a pair waits a fixed time instead: far longer than a copy
+      // takes to land (microseconds), and both CTAs then still pass the exit
+      // handshake, so neither leaves while the other's copies may land.
+      if constexpr (kPair) {
+        const uint64_t t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < kPairCopyDrainNs) {
+        }
+      } else {
+        for (int s = 0; s < STAGES; ++s)
+          if ((filled >> s) & 1u) drain_wait(bar_full + 8 * s, (fill_phase >> s) & 1u);
+      }
     } else if constexpr (kPair) {
       // every stage's last use released by the even CTA's MMAs (whose commits
       // arrive on this CTA's barriers) before the CTA may exit
@@ -483,13 +519,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_full + 8 * slot);
+      if (lane == 0) {
+        // pairs: on the even CTA's barrier (the odd CTA's stores are complete,
+        // waited for above, so a relaxed arrive has nothing left to order)
+        if (kPair && rank == 1) mbar_remote_arrive_relaxed(pair_full0 + 8 * slot);
+        else mbar_arrive(bar_full + 8 * slot);
+      }
     }
     // After an abort the stages this warp did not process still get its
     // arrival, so that the producer's drain of its copies in flight (a wait on
     // the same barriers) completes as soon as they land.
     if (!ok && lane == 0)
-      for (int i = 0; i < STAGES && g + i < nstages; ++i) mbar_arrive(bar_full + 8 * ((g + i) % STAGES));
+      for (int i = 0; i < STAGES && g + i < nstages; ++i) {
+        const int slot = (g + i) % STAGES;
+        if (kPair && rank == 1) mbar_remote_arrive_relaxed(pair_full0 + 8 * slot);
+        else mbar_arrive(bar_full + 8 * slot);
+      }
   } else if (warp == 1 && lane == 0 && rank == 0) {
     // ---------------------------------------------------------------- MMA issuer
     uint32_t stage = 0, phase = 0, aphase = 0;
@@ -510,17 +555,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         sch.decode(t, 0, e, nb, mb, rows, ncols);
         idesc = idesc_nvf4(BM, ncols);
       }
-      if (!wait_bounded(bar_acce, aphase ^ 1, abort_flag, p.wait_limit_ns, p.status, 2, peer_abort) ||
-          (kPair && !wait_bounded<true>(bar_peer_acce, aphase ^ 1, abort_flag, p.wait_limit_ns, p.status, 11,
-                                        peer_abort))) {
+      // pairs: both CTAs' epilogues arrive on this barrier
+      if (!wait_bounded<kPair>(bar_acce, aphase ^ 1, abort_flag, p.wait_limit_ns, p.status, 2, peer_abort)) {
         ok = false;
         break;
       }
       tc_fence_after();
       for (int kb = 0; kb < kblocks; ++kb) {
-        if (!wait_bounded(bar_full + 8 * stage, phase, abort_flag, p.wait_limit_ns, p.status, 7, peer_abort) ||
-            (kPair && !wait_bounded<true>(bar_peer_full + 8 * stage, phase, abort_flag, p.wait_limit_ns, p.status,
-                                          12, peer_abort))) {
+        // pairs: both CTAs' code tiles and scale warps complete this barrier
+        if (!wait_bounded<kPair>(bar_full + 8 * stage, phase, abort_flag, p.wait_limit_ns, p.status, 7,
+                                 peer_abort)) {
           ok = false;
           break;
         }
@@ -571,33 +615,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       else tc_commit(bar_aux);
       drain_wait(bar_aux, 0);
     }
-  } else if (kPair && warp == 1 && lane == 0) {
-    // ---------------------------------------------------------------- pair relay (odd CTA)
-    // Tells the even CTA's MMA issuer, in the order it consumes them, that this
-    // CTA's stage is loaded and its scales are in tensor memory, and that this
-    // CTA's epilogue has released the accumulator of the previous unit.
-    const uint32_t r_peer_full = mapa_shared(bar_peer_full, 0);
-    const uint32_t r_peer_acce = mapa_shared(bar_peer_acce, 0);
-    uint32_t stage = 0, phase = 0, aph = 0;
-    bool ok = true;
-    for (int i = 0; ok && i < my_units; ++i) {
-      if (i > 0) {
-        if (!wait_bounded(bar_acce, aph, abort_flag, p.wait_limit_ns, p.status, 13, peer_abort)) break;
-        aph ^= 1;
-        mbar_remote_arrive_relaxed(r_peer_acce);
-      }
-      for (int kb = 0; kb < kblocks; ++kb) {
-        if (!wait_bounded(bar_full + 8 * stage, phase, abort_flag, p.wait_limit_ns, p.status, 15, peer_abort)) {
-          ok = false;
-          break;
-        }
-        mbar_remote_arrive_relaxed(r_peer_full + 8 * stage);
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1;
-        }
-      }
-    }
   } else if (warp >= kFirstEpiWarp && warp < kFirstEpiWarp + kEpiWarps) {
     // ---------------------------------------------------------------- epilogue
     const int quad = warp & 3;                 // TMEM lane quadrant this warp may access
@@ -605,6 +622,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = quad * 32 + lane;
     uint32_t aphase = 0;
     const float gs_a = *p.gs_a;
+    // The accumulator is released on the barrier the MMA issuer waits on:
+    // pairs' odd CTA with one relaxed remote arrive per warp, after every
+    // lane's tensor-memory loads were waited for.
+    auto release_acc = [&]() {
+      if (kPair && rank == 1) {
+        __syncwarp();
+        if (lane == 0) mbar_remote_arrive_relaxed(pair_acce);
+      } else {
+        mbar_arrive(bar_acce);
+      }
+    };
     for (int t = first_unit; t < total; t += unit_stride) {
       int e, nb, mb, rows, ncols;
       sch.decode(t, rank, e, nb, mb, rows, ncols);
@@ -630,7 +658,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         tc_fence_before();
-        mbar_arrive(bar_acce);
+        release_acc();
         if (!active) continue;
         const int64_t orow = (int64_t)p.offsets[e] + mb * BM + row;
         __nv_bfloat16* out = p.c + orow * p.ldc + nb * BN + half * 128;
@@ -671,7 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_ld64_wait(taddr + 64, u1);
         const float* v1 = reinterpret_cast<const float*>(u1);
         tc_fence_before();
-        mbar_arrive(bar_acce);
+        release_acc();
         if (!active) continue;
         const float gs_h = *p.gs_h;
         const int64_t hrow = (int64_t)pad_off[e] + mb * BM + row;

@@ -35,10 +35,13 @@ KERNELS_PER_STEP_FUSED = 4         # fused dispatch 1, L1 1, L2 1, combine 1 (st
 
 
 def kernels_per_step(T, k, fused):
-    """Kernels of one moe_forward: the fused dispatch path, else route 1,
-    permute 1 (up to 1024 slots) or 3, quantize 3, L1 1, L2 1, combine 1."""
+    """Kernels of one moe_forward: the fused dispatch path (its quantize +
+    scatter a second kernel above B.FRONT_FUSED_QUANTIZE_MAX_ROWS routed
+    rows), else route 1, permute 1 (up to 1024 slots) or 3, quantize 3, L1 1,
+    L2 1, combine 1."""
+    from nvfp4_block_scaled_05_gb300 import binding as B
     if fused:
-        return KERNELS_PER_STEP_FUSED
+        return KERNELS_PER_STEP_FUSED + (1 if T * k > B.FRONT_FUSED_QUANTIZE_MAX_ROWS else 0)
     return 1 + (1 if T * k <= 1024 else 3) + 3 + 3
 
 
@@ -622,7 +625,10 @@ def run_ours(args, cfg):
                    "active_experts": nums["active"], "seed": args.seed, "gs_h": cfg.gs_h,
                    "front": ("static (moe_forward_static; gs_x pre-computed once by a calibration "
                              "forward)" if static else
-                             ("fused dispatch kernel (gs_x computed every step)" if fused_front else
+                             (("fused dispatch kernel (gs_x computed every step)"
+                               if T * k <= B.FRONT_FUSED_QUANTIZE_MAX_ROWS else
+                               "fused routing + permutation kernel, then the quantize + scatter kernel "
+                               "(gs_x computed every step)") if fused_front else
                               "route, permute and quantize kernels (gs_x computed every step)")),
                    "cuda_graph": bool(args.graph),
                    "gemm_kernel": "2-SM pairs" if args.gemm_mode == 1 else "one CTA per tile",

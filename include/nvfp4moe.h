@@ -101,6 +101,11 @@ enum {
 #define NVFP4_SF_TILED 1
 #define NVFP4_SF_TILED_ROWS 2
 
+/* Routed rows (T * k) up to which moe_dispatch and moe_dispatch_static do the
+ * quantize + scatter inside their cooperative kernel; above, a second kernel
+ * does it (measured faster there). */
+#define NVFP4MOE_FRONT_FUSED_QUANTIZE_MAX_ROWS 32768
+
 /* Short description of a status code (static string). */
 const char* nvfp4moe_status_string(int status);
 
@@ -388,7 +393,7 @@ int moe_forward_workspace_layout(int64_t T, int64_t K, int64_t I, int E, int k,
  *   ws             >= moe_forward_workspace_size(T, K, I, E, k) bytes,
  *                  256-byte aligned.
  * Requires K % 128 == 0, I % 64 == 0, 1 <= k <= 16, k <= E <= 1024, T >= 0.
- * Stages 1-2 run as moe_dispatch (one cooperative kernel) when
+ * Stages 1-2 run as moe_dispatch (the fused front) when
  * moe_forward_uses_fused_dispatch(T, E, k), else as moe_route_topk,
  * moe_permute and moe_quantize_dispatch; the intermediates are the same bit
  * for bit. Then the
@@ -409,9 +414,12 @@ size_t moe_dispatch_static_workspace_size(int64_t T, int E);
  * moe_dispatch_static -- stages 1 and 2 fused, with a pre-computed activation
  * global scale *gs_x (README "Bridge Layer": quantize_activation_nvfp4 with
  * pre-computed gs; "MoE Runner" steps 1-2): moe_route_topk, moe_permute and
- * moe_quantize_dispatch (with gs_in = gs_x) in ONE cooperative kernel with
+ * moe_quantize_dispatch (with gs_in = gs_x) in one cooperative kernel with
  * two grid-wide barriers, each bounded by the wait limit (a timeout sets the
- * device status; offsets and flat_to_perm are then all zero).
+ * device status; offsets and flat_to_perm are then all zero, so every slot's
+ * codes land in padded row 0). Above NVFP4MOE_FRONT_FUSED_QUANTIZE_MAX_ROWS
+ * routed rows the cooperative kernel stops after the permutation and a
+ * second kernel does the quantize + scatter (the same bits).
  * Outputs as those three calls: topk_ids / topk_w (T, k); offsets (E + 1);
  * perm_to_flat / flat_to_perm (T*k); a_codes / a_sf in the grouped-padded
  * rows of (a_rows, K) with a_rows >= nvfp4moe_padded_rows(T*k, E).
@@ -430,9 +438,9 @@ int moe_dispatch_static(const void* x, int64_t ldx, const float* router_logits, 
  * only (queries the device's occupancy). */
 int moe_dispatch_supported(int64_t T, int E, int k);
 
-/* 1 if moe_forward runs stages 1-2 as moe_dispatch for this shape: when
- * moe_dispatch_supported and T * k <= 65536 (above that the separate kernels
- * are faster), else 0. Host only. */
+/* 1 if moe_forward runs stages 1-2 as moe_dispatch for this shape: whenever
+ * moe_dispatch_supported, else 0 (the separate moe_route_topk, moe_permute
+ * and moe_quantize_dispatch). Host only. */
 int moe_forward_uses_fused_dispatch(int64_t T, int E, int k);
 
 /*

@@ -16,6 +16,9 @@ from . import build as _build
 NVFP4_SF_ROWMAJOR = 0
 NVFP4_SF_TILED = 1          # weight (B) operand scales of the GEMMs
 NVFP4_SF_TILED_ROWS = 2     # activation (A) operand scales of the GEMMs
+# include/nvfp4moe.h NVFP4MOE_FRONT_FUSED_QUANTIZE_MAX_ROWS: routed rows up to
+# which the fused dispatch quantizes inside its cooperative kernel
+FRONT_FUSED_QUANTIZE_MAX_ROWS = 32768
 
 _c_void_p = ctypes.c_void_p
 _i64 = ctypes.c_int64
@@ -453,8 +456,8 @@ def moe_forward_uses_fused_dispatch(T, E, k):
 
 
 def forward_stages(T, E, k):
-    """The stages moe_forward runs for this shape: the fused dispatch kernel,
-    or the separate route, permute and quantize."""
+    """The stages moe_forward runs for this shape: the fused dispatch (one
+    call), or the separate route, permute and quantize."""
     return FUSED_STAGES if moe_forward_uses_fused_dispatch(T, E, k) else SPLIT_STAGES
 
 

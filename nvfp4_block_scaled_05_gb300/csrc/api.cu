@@ -220,12 +220,13 @@ extern "C" int moe_dispatch_static(const void* x, int64_t ldx, const float* rout
 
 extern "C" int moe_dispatch_supported(int64_t T, int E, int k) { return moe_front_fits(T, E, k) ? 1 : 0; }
 
-// Measured on GB300: the fused dispatch saves the separate launches up to
-// 65536 routed rows (decode: 21 us against 38 us; 65536 rows: 0.144 ms) and
-// is slower above (131072 rows: 0.28 against 0.25 ms), where the separate
-// kernels' full-occupancy grids stream x faster than its co-resident blocks.
+// Measured on GB300: the fused dispatch (with its quantize + scatter as a
+// second kernel above NVFP4MOE_FRONT_FUSED_QUANTIZE_MAX_ROWS routed rows) is
+// faster than the separate route/permute/quantize at every size measured
+// (1024 rows: 20 against 36 us; 32768 rows: 63 against 89 us; 65536 rows:
+// 122 against 147 us; 131072 rows: 224 against 250 us).
 extern "C" int moe_forward_uses_fused_dispatch(int64_t T, int E, int k) {
-  return T >= 1 && T * k <= 65536 && moe_front_fits(T, E, k) ? 1 : 0;
+  return T >= 1 && moe_front_fits(T, E, k) ? 1 : 0;
 }
 
 extern "C" int moe_dispatch(const void* x, int64_t ldx, const float* router_logits, int64_t T, int64_t K,

@@ -20,13 +20,24 @@
 //            __match_any_sync), then each token row is quantized once and
 //            written to the padded rows of its k slots (gs = 2688 / max|x|
 //            when it was not given).
+// Above NVFP4MOE_FRONT_FUSED_QUANTIZE_MAX_ROWS routed rows the kernel stops
+// after the stable positions (block 0 writes the padded group starts) and the
+// quantize + scatter runs as a second, full-occupancy kernel (the one of
+// moe_quantize_dispatch). Measured on GB300: in the cooperative kernel that
+// phase is latency-bound at 2 blocks of 512 threads per SM (64 registers),
+// 4.2-4.6 TB/s, against 5.1 TB/s for the separate kernel (one 512-element
+// item per warp, 48 warps per SM); the second launch costs ~4 us. Front
+// times, quantize inside / as a second kernel: 1024 rows 20 / 24 us, 8192
+// rows 27 / 28 us, 32768 rows 63 / 64 us, 65536 rows 138 / 122 us, 131072
+// rows 270 / 224 us.
 // The same permutation as moe_permute (a stable counting sort by expert of
 // the flat slots t*k + j), the same rows as moe_quantize_dispatch.
 //
 // The grid barriers are bounded: one that does not complete within the wait
 // limit sets the device status to NVFP4MOE_ERR_DEVICE_TIMEOUT (wait site 8 or
-// 9) and the kernel returns. Offsets and flat_to_perm are zeroed before the first barrier, so
-// the later stages then find no rows and read nothing out of bounds.
+// 9) and the kernel returns. Offsets, flat_to_perm (and the padded group
+// starts when a second kernel quantizes) are zeroed before the first barrier,
+// so the later stages then find no rows and read nothing out of bounds.
 #include "common.cuh"
 
 namespace nvfp4moe {
@@ -54,6 +65,8 @@ struct FrontParams {
   uint8_t* a_sf;
   int32_t* counts;        // [G][E]
   int32_t* totals;        // [E]
+  int32_t* pad_out;       // [E] padded group starts, written when !quantize
+  int quantize;           // 1: quantize + scatter here; 0: stop after the positions
   unsigned int* barrier;  // zeroed before the launch
   uint64_t limit_ns;
   int* status;
@@ -138,8 +151,11 @@ __global__ void __launch_bounds__(kFrontThreads) moe_front_kernel(const FrontPar
 
   // ---- phase 1: route, histogram; safe offsets / flat_to_perm first
   for (int e = tid; e < E; e += kFrontThreads) next[e] = 0;
-  if (c == 0)
+  if (c == 0) {
     for (int e = tid; e <= E; e += kFrontThreads) p.offsets[e] = 0;
+    if (!p.quantize)   // read by the quantize kernel that follows, even after a timeout
+      for (int e = tid; e < E; e += kFrontThreads) p.pad_out[e] = 0;
+  }
   for (int s = tid; s < nslot; s += kFrontThreads) p.f2p[t0 * k + s] = 0;
   __syncthreads();
   for (int tl = warp; tl < ntok; tl += nwarps) {
@@ -240,6 +256,11 @@ __global__ void __launch_bounds__(kFrontThreads) moe_front_kernel(const FrontPar
     }
   }
   __syncthreads();
+  if (!p.quantize) {
+    if (c == 0)
+      for (int e = tid; e < E; e += kFrontThreads) p.pad_out[e] = pad[e];
+    return;
+  }
   const float gs = p.gs_x ? *p.gs_x : global_scale_from_amax_bits(__ldcg(p.amax_bits));
   if (p.gs_out && c == 0 && tid == 0) *p.gs_out = gs;
   const int nchunk = (p.K + 511) / 512;
@@ -329,7 +350,7 @@ int vpl_of(int E) { return E <= 32 ? 1 : E <= 64 ? 2 : E <= 128 ? 4 : E <= 256 ?
 
 size_t front_workspace_bytes(int64_t T, int E) {
   const int64_t g = T < kFrontMaxBlocks ? T : kFrontMaxBlocks;
-  return 256 + (size_t)ceil_div((int64_t)E * 4, 256) * 256 + (size_t)ceil_div(g * E * 4, 256) * 256;
+  return 256 + 2 * (size_t)ceil_div((int64_t)E * 4, 256) * 256 + (size_t)ceil_div(g * E * 4, 256) * 256;
 }
 
 bool moe_front_fits(int64_t T, int E, int k) {
@@ -382,22 +403,32 @@ int moe_front(const void* x, int64_t ldx, const float* logits, int64_t T, int64_
   uint8_t* wb = static_cast<uint8_t*>(ws);
   p.barrier = reinterpret_cast<unsigned int*>(wb);
   p.amax_bits = reinterpret_cast<uint32_t*>(wb + 4);
+  const int64_t e_bytes = ceil_div((int64_t)E * 4, 256) * 256;
   p.totals = reinterpret_cast<int32_t*>(wb + 256);
-  p.counts = reinterpret_cast<int32_t*>(wb + 256 + ceil_div((int64_t)E * 4, 256) * 256);
+  p.pad_out = reinterpret_cast<int32_t*>(wb + 256 + e_bytes);
+  p.counts = reinterpret_cast<int32_t*>(wb + 256 + 2 * e_bytes);
+  p.quantize = T * k <= NVFP4MOE_FRONT_FUSED_QUANTIZE_MAX_ROWS ? 1 : 0;
   p.limit_ns = wait_limit_ns();
   p.status = device_status_word();
   p.test_stall = test_stall_on();
   NVFP4_CHECK(p.status, NVFP4MOE_ERR_LAUNCH);
   if (cudaMemsetAsync(p.barrier, 0, 2 * sizeof(unsigned int), s) != cudaSuccess) return NVFP4MOE_ERR_LAUNCH;
   const size_t smem = front_smem_bytes(E, tpb * k);
+  int st;
   switch (vpl) {
-    case 1: return launch_front_vpl<1>(p, G, smem, s);
-    case 2: return launch_front_vpl<2>(p, G, smem, s);
-    case 4: return launch_front_vpl<4>(p, G, smem, s);
-    case 8: return launch_front_vpl<8>(p, G, smem, s);
-    case 16: return launch_front_vpl<16>(p, G, smem, s);
-    default: return launch_front_vpl<32>(p, G, smem, s);
+    case 1: st = launch_front_vpl<1>(p, G, smem, s); break;
+    case 2: st = launch_front_vpl<2>(p, G, smem, s); break;
+    case 4: st = launch_front_vpl<4>(p, G, smem, s); break;
+    case 8: st = launch_front_vpl<8>(p, G, smem, s); break;
+    case 16: st = launch_front_vpl<16>(p, G, smem, s); break;
+    default: st = launch_front_vpl<32>(p, G, smem, s); break;
   }
+  if (st != NVFP4MOE_OK || p.quantize) return st;
+  // After a barrier timeout the cooperative kernel leaves offsets and
+  // flat_to_perm zeroed, so this kernel then finds every slot in expert 0's
+  // first rows: it writes only inside the padded operand and reads only x.
+  return launch_dispatch_quantize(x, T, K, ldx, k, gs_x, gs_x ? nullptr : p.amax_bits, gs_out, ids, offsets,
+                                  f2p, p.pad_out, a_codes, a_sf, s);
 }
 
 }  // namespace nvfp4moe

@@ -424,6 +424,20 @@ extern "C" int nvfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t
   return launch_status();
 }
 
+namespace nvfp4moe {
+int launch_dispatch_quantize(const void* x, int64_t T, int64_t K, int64_t ldx, int k, const float* gs_in,
+                             const uint32_t* amax_bits, float* gs_out, const int32_t* topk_ids,
+                             const int32_t* offsets, const int32_t* flat_to_perm, const int32_t* pad_off,
+                             uint8_t* a_codes, uint8_t* a_sf, cudaStream_t s) {
+  if (T == 0) return NVFP4MOE_OK;
+  const int64_t warps = T * ceil_div(K, kChunk);
+  dispatch_quantize_kernel<<<(unsigned)ceil_div(warps, kWarpsPerBlock), 256, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(x), T, K, ldx, k, gs_in, amax_bits, gs_out, topk_ids, offsets,
+      flat_to_perm, pad_off, a_codes, a_sf);
+  return launch_status();
+}
+}  // namespace nvfp4moe
+
 extern "C" int moe_quantize_dispatch(const void* x, int64_t T, int64_t K, int64_t ldx, int k, int E,
                                      const int32_t* topk_ids, const int32_t* offsets,
                                      const int32_t* flat_to_perm, const float* gs_in,
@@ -444,11 +458,8 @@ extern "C" int moe_quantize_dispatch(const void* x, int64_t T, int64_t K, int64_
   NVFP4_TRY(launch_status());
   if (T == 0) return NVFP4MOE_OK;
   if (!gs_in) NVFP4_TRY(launch_amax(x, T, K, ldx, nullptr, amax_bits, s));
-  const int64_t warps = T * ceil_div(K, kChunk);
-  dispatch_quantize_kernel<<<(unsigned)ceil_div(warps, kWarpsPerBlock), 256, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(x), T, K, ldx, k, gs_in, gs_in ? nullptr : amax_bits,
-      gs_out, topk_ids, offsets, flat_to_perm, pad_off, a_codes, a_sf);
-  return launch_status();
+  return launch_dispatch_quantize(x, T, K, ldx, k, gs_in, gs_in ? nullptr : amax_bits, gs_out, topk_ids, offsets,
+                                  flat_to_perm, pad_off, a_codes, a_sf, s);
 }
 
 extern "C" int nvfp4_rmsnorm_rope_quantize(const void* x, int64_t rows, int64_t D, int64_t ldx,

@@ -31,6 +31,18 @@ def test_header_declares_the_entry_points():
         assert must in names
 
 
+def test_binding_constants_match_the_header():
+    """The binding's copies of the header's #define constants (bench.py counts
+    the front's launches from the threshold)."""
+    from nvfp4_block_scaled_05_gb300 import binding as B
+    with open(os.path.join(ROOT, "include", "nvfp4moe.h")) as f:
+        text = f.read()
+    defs = dict(re.findall(r"#define (NVFP4\w+) (\d+)", text))
+    assert int(defs["NVFP4MOE_FRONT_FUSED_QUANTIZE_MAX_ROWS"]) == B.FRONT_FUSED_QUANTIZE_MAX_ROWS
+    for name in ("NVFP4_SF_ROWMAJOR", "NVFP4_SF_TILED", "NVFP4_SF_TILED_ROWS"):
+        assert int(defs[name]) == getattr(B, name)
+
+
 def test_library_exports_every_declared_symbol(lib):
     for name in _declared():
         assert hasattr(lib, name), name

@@ -170,13 +170,16 @@ def test_moe_largest_expert_count_and_topk():
 
 
 def test_fused_dispatch_choice():
-    """moe_forward takes the fused dispatch kernel up to 65536 routed rows and
-    the separate kernels above."""
-    assert B.moe_forward_uses_fused_dispatch(128, 256, 8)
-    assert B.moe_forward_uses_fused_dispatch(8192, 256, 8)
-    assert not B.moe_forward_uses_fused_dispatch(8193, 256, 8)
-    assert not B.moe_forward_uses_fused_dispatch(16384, 256, 8)
-    assert B.moe_dispatch_supported(16384, 256, 8)
+    """moe_forward takes the fused dispatch whenever its cooperative kernel's
+    co-resident blocks hold the tokens (above FRONT_FUSED_QUANTIZE_MAX_ROWS
+    routed rows its quantize + scatter is a second kernel), and the separate
+    kernels beyond that."""
+    for T in (1, 128, 8192, 16384):
+        assert B.moe_forward_uses_fused_dispatch(T, 256, 8)
+        assert B.moe_dispatch_supported(T, 256, 8)
+    # 1.6M routed rows: more than 4096 slots per co-resident block
+    assert not B.moe_dispatch_supported(200000, 256, 8)
+    assert not B.moe_forward_uses_fused_dispatch(200000, 256, 8)
 
 
 def test_moe_skewed_heaviest_expert_every_tile():

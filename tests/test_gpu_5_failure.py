@@ -59,15 +59,24 @@ def test_wait_timeout_is_reported_and_context_survives(mode):
     assert torch.isfinite(good.float()).all()
 
 
-@pytest.mark.parametrize("front", ["static", "dynamic"])
-def test_front_barrier_timeout_is_reported_and_context_survives(front):
+@pytest.mark.parametrize("front,size", [("static", "tiny"), ("dynamic", "tiny"), ("static", "big"),
+                                       ("dynamic", "big")])
+def test_front_barrier_timeout_is_reported_and_context_survives(front, size):
     """The fused front (moe_forward_static with its given global scale, or
     moe_forward, whose dispatch computes it): with the test stall on, block 0
     leaves before the first grid barrier; the other blocks' bounded barrier
     waits run out, the status reads NVFP4MOE_ERR_DEVICE_TIMEOUT, the later
-    stages find no rows, and the next normal call gives the normal result."""
+    stages find no rows, and the next normal call gives the normal result.
+    "big" has more routed rows than FRONT_FUSED_QUANTIZE_MAX_ROWS, so the
+    quantize + scatter runs as a second kernel after the timed-out one (on the
+    zeroed offsets, positions and padded starts: every slot into row 0)."""
     from nvfp4_block_scaled_05_gb300 import workloads as W
-    cfg = W.CONFIGS["tiny"]
+    if size == "tiny":
+        cfg = W.CONFIGS["tiny"]
+    else:
+        T = B.FRONT_FUSED_QUANTIZE_MAX_ROWS // 8 + 64
+        cfg = W.MoEConfig("big", T=T, K=256, I=128, E=8, k=8, gs_h=1344.0)
+        assert T * cfg.k > B.FRONT_FUSED_QUANTIZE_MAX_ROWS
     inp = W.moe_inputs(cfg, seed=4, device=DEV)
     wts = B.prepare_moe_weights(inp["w1"], inp["w2"])
     gs_h = torch.tensor([cfg.gs_h], dtype=torch.float32, device=DEV)

@@ -199,8 +199,9 @@ def _split_and_fused(cfg, x, logits):
 
 @pytest.mark.parametrize("name", ["tiny", "decode", "prefill", "skewed", "dsv4_decode"])
 def test_fused_dispatch_equals_separate_calls(name):
-    """moe_dispatch (one cooperative kernel, the global scale of x computed in
-    it) writes the same bits as moe_route_topk + moe_permute +
+    """moe_dispatch (the cooperative kernel, the global scale of x computed in
+    it; prefill and skewed with the quantize + scatter as a second kernel)
+    writes the same bits as moe_route_topk + moe_permute +
     moe_quantize_dispatch: routing, permutation, offsets, gs_x, and every
     routed row's codes and scales."""
     cfg = W.CONFIGS[name]
@@ -235,6 +236,23 @@ def test_fused_dispatch_edge_shapes():
             assert fused["gs_x"] == O.global_scale(O.amax_bf16(W.bf16_bits(x))) == np.float32(2688.0 / 40.0)
         for n in NAMES + ["rows", "sf"]:
             assert np.array_equal(fused[n], split[n]), (n, T, E)
+
+
+@pytest.mark.parametrize("extra", [0, 1])
+def test_fused_dispatch_at_the_quantize_kernel_threshold(extra):
+    """T * k exactly FRONT_FUSED_QUANTIZE_MAX_ROWS (quantize + scatter inside
+    the cooperative kernel) and one token more (the second kernel): the same
+    bits as the separate calls, with the global scale computed."""
+    k = 8
+    T = B.FRONT_FUSED_QUANTIZE_MAX_ROWS // k + extra
+    cfg = W.MoEConfig("threshold", T=T, K=384, I=64, E=24, k=k, gs_h=336.0)
+    g = torch.Generator(device="cpu").manual_seed(T)
+    x = torch.randn(T, 384, generator=g).to(torch.bfloat16)
+    logits = torch.randn(T, 24, generator=g)
+    split, fused = _split_and_fused(cfg, x.to(DEV), logits.to(DEV))
+    assert fused["gs_x"] == split["gs_x"]
+    for n in NAMES + ["rows", "sf"]:
+        assert np.array_equal(fused[n], split[n]), n
 
 
 def test_fused_dispatch_nan_logits():

@@ -287,14 +287,16 @@ def time_oracle(cfg, sample):
     return dt, flops
 
 
-def full_size_parity(cfg, seed, n_experts, x, logits, dev, f2p, out, topk_w):
+def full_size_parity(cfg, seed, n_experts, x, logits, dev, f2p, out, topk_w, max_rows=None):
     """Parity of the benchmarked run itself on a bounded sample: for every token
     routed to one of n_experts active experts, those experts' share of y,
     sum_j w[t,j] * out[t,j] over the slots j routed to them, formed from the
     L2 output rows and routing weights left in the workspace by the last timed
     forward, against the oracle's fp64 share on the same inputs (x and logits
     copied back, the sampled experts' weights drawn again on the device: the
-    same values as the run's), with the layer tolerance (2e-2 * max(1, |y|))."""
+    same values as the run's), with the layer tolerance (2e-2 * max(1, |y|)).
+    max_rows: only experts with at most that many routed rows are sampled (the
+    first n_experts of them in index order), which bounds the oracle's time."""
     import numpy as np
     import oracle as O
     from nvfp4_block_scaled_05_gb300 import workloads as W
@@ -302,7 +304,8 @@ def full_size_parity(cfg, seed, n_experts, x, logits, dev, f2p, out, topk_w):
     lg = logits.cpu().numpy()
     ids = O.route_topk(lg, cfg.k)[0]
     counts = np.bincount(ids.ravel(), minlength=cfg.E)
-    experts = [e for e in range(cfg.E) if counts[e] > 0][:n_experts]
+    experts = [e for e in range(cfg.E) if counts[e] > 0 and (max_rows is None or counts[e] <= max_rows)]
+    experts = experts[:n_experts]
     qw = {}
     for e in experts:
         c1, s1, g1 = O.quantize_expert(W.bf16_bits(W.expert_weight(cfg, seed, 1, e, dev).cpu()))
@@ -727,6 +730,16 @@ def measure_also(args, base, wts, dev, hbm_peak, fp4_peak):
                     for j, n in enumerate(names)}
         lay = B.moe_forward_workspace_layout(T, K, I, E, k)
         offsets = ws[lay["offsets"]:lay["offsets"] + 4 * (E + 1)].view(torch.int32).cpu().tolist()
+        parity = None
+        if not args.no_cpu_baseline:
+            # the last forward's L2 rows and routing against the oracle, as for
+            # the benchmarked workload (a bounded sample of experts)
+            M = T * k
+            f2p_h = ws[lay["flat_to_perm"]:lay["flat_to_perm"] + 4 * M].view(torch.int32).cpu().numpy()
+            out_h = ws[lay["out"]:lay["out"] + 2 * M * K].view(torch.int16).view(M, K).cpu().numpy().view("uint16")
+            tw_h = ws[lay["topk_w"]:lay["topk_w"] + 4 * M].view(torch.float32).cpu().numpy()
+            parity, _ = full_size_parity(cfg, args.seed, 8 if name == "decode" else 4, x, logits, dev,
+                                         f2p_h, out_h, tw_h, max_rows=None if name == "decode" else 600)
         nums = layer_numbers(cfg, offsets)
         roof = l1_roofline(nums, stage_ms["l1_swiglu"], hbm_peak, fp4_peak)
         tf = nums["flops"] / (ms * 1e-3) / 1e12
@@ -737,6 +750,8 @@ def measure_also(args, base, wts, dev, hbm_peak, fp4_peak):
                                      "unit": roof["unit"], "kernel_ms": stage_ms["l1_swiglu"],
                                      "traffic": ncu_traffic(name)},
                      "clocks": clk}
+        if parity is not None:
+            out[name]["parity"] = parity
         del ws, y, x, logits
         torch.cuda.empty_cache()
     return out

@@ -54,14 +54,6 @@ int moe_front(const void* x, int64_t ldx, const float* logits, int64_t T, int64_
               const float* gs_x, float* gs_out, int32_t* ids, float* w, int32_t* offsets, int32_t* p2f,
               int32_t* f2p, uint8_t* a_codes, uint8_t* a_sf, void* ws, size_t ws_bytes, cudaStream_t s);
 
-// Quantize + scatter of moe_quantize_dispatch (quantize.cu), given the padded
-// group starts pad_off[e] (e < E) and either gs_in or the bits of max|x| (the
-// global scale is then 2688 / max|x|, written to gs_out when that is not null).
-int launch_dispatch_quantize(const void* x, int64_t T, int64_t K, int64_t ldx, int k, const float* gs_in,
-                             const uint32_t* amax_bits, float* gs_out, const int32_t* topk_ids,
-                             const int32_t* offsets, const int32_t* flat_to_perm, const int32_t* pad_off,
-                             uint8_t* a_codes, uint8_t* a_sf, cudaStream_t s);
-
 // Byte offset of the scale of (row r, 16-element block b) in the tiled layout
 // documented in nvfp4moe.h.
 // It is the sum of a row part and a block part (c4 = column groups of 64).

@@ -41,6 +41,16 @@
 #include "common.cuh"
 
 namespace nvfp4moe {
+
+// Quantize + scatter of moe_quantize_dispatch (defined in quantize.cu), given
+// the padded group starts pad_off[e] (e < E) and either gs_in or the bits of
+// max|x| (the global scale is then 2688 / max|x|, written to gs_out when that
+// is not null).
+int launch_dispatch_quantize(const void* x, int64_t T, int64_t K, int64_t ldx, int k, const float* gs_in,
+                             const uint32_t* amax_bits, float* gs_out, const int32_t* topk_ids,
+                             const int32_t* offsets, const int32_t* flat_to_perm, const int32_t* pad_off,
+                             uint8_t* a_codes, uint8_t* a_sf, cudaStream_t s);
+
 namespace {
 
 constexpr int kFrontThreads = 512;

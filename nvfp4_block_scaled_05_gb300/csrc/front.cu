@@ -434,9 +434,9 @@ int moe_front(const void* x, int64_t ldx, const float* logits, int64_t T, int64_
     default: st = launch_front_vpl<32>(p, G, smem, s); break;
   }
   if (st != NVFP4MOE_OK || p.quantize) return st;
-  // After a barrier timeout the cooperative kernel leaves offsets and
-  // flat_to_perm zeroed, so this kernel then finds every slot in expert 0's
-  // first rows: it writes only inside the padded operand and reads only x.
+  // After a barrier timeout the cooperative kernel leaves offsets,
+  // flat_to_perm and the padded starts zeroed, so this kernel writes every
+  // slot into padded row 0: only inside the padded operand.
   return launch_dispatch_quantize(x, T, K, ldx, k, gs_x, gs_x ? nullptr : p.amax_bits, gs_out, ids, offsets,
                                   f2p, p.pad_out, a_codes, a_sf, s);
 }

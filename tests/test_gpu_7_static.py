@@ -130,8 +130,17 @@ def test_static_edge_shapes():
         assert torch.equal(y1, y2), (T, E, k)
 
 
-def test_static_graph_replay_on_new_inputs():
-    cfg = W.CONFIGS["decode"]
+@pytest.mark.parametrize("name", ["decode", "front_two_kernels"])
+def test_static_graph_replay_on_new_inputs(name):
+    """moe_forward_static captured in a CUDA graph and replayed on new inputs
+    copied into the captured buffers equals the eager call bit for bit.
+    "front_two_kernels" has more routed rows than FRONT_FUSED_QUANTIZE_MAX_ROWS,
+    so the captured front is the cooperative kernel plus the quantize kernel."""
+    if name == "decode":
+        cfg = W.CONFIGS["decode"]
+    else:
+        T = B.FRONT_FUSED_QUANTIZE_MAX_ROWS // 8 + 40
+        cfg = W.MoEConfig(name, T=T, K=256, I=128, E=16, k=8, gs_h=1344.0)
     inp, wts, gs_h, nb, lay = _setup(cfg, seed=2)
     inp2 = W.moe_inputs(cfg, seed=3, device=DEV, weights=False)
     gs_x = torch.tensor([2688.0 / 4.5], dtype=torch.float32, device=DEV)
@@ -152,6 +161,37 @@ def test_static_graph_replay_on_new_inputs():
         graph.replay()
         torch.cuda.synchronize()
         eager = B.moe_forward_static(src["x"], src["logits"], wts, cfg.k, gs_h, gs_x)
+        assert B.nvfp4moe_last_device_status() == 0
+        assert torch.equal(y_s, eager)
+
+
+def test_dynamic_graph_replay_two_kernel_front():
+    """moe_forward (the global scale of x computed every call) captured in a
+    CUDA graph at more routed rows than FRONT_FUSED_QUANTIZE_MAX_ROWS (the
+    front's counter reset, cooperative kernel and quantize kernel are all
+    graph nodes), replayed on new inputs: bit for bit the eager result."""
+    T = B.FRONT_FUSED_QUANTIZE_MAX_ROWS // 8 + 40
+    cfg = W.MoEConfig("front_two_kernels", T=T, K=256, I=128, E=16, k=8, gs_h=1344.0)
+    assert B.moe_forward_uses_fused_dispatch(cfg.T, cfg.E, cfg.k)
+    inp, wts, gs_h, nb, lay = _setup(cfg, seed=6)
+    inp2 = W.moe_inputs(cfg, seed=7, device=DEV, weights=False)
+    ws = torch.empty(nb, dtype=torch.uint8, device=DEV)
+    x_s, l_s = inp["x"].clone(), inp["logits"].clone()
+    y_s = torch.empty_like(inp["x"])
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        B.moe_forward(x_s, l_s, wts, cfg.k, gs_h, ws=ws, y=y_s)   # warm-up
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            B.moe_forward(x_s, l_s, wts, cfg.k, gs_h, ws=ws, y=y_s)
+    torch.cuda.current_stream().wait_stream(s)
+    for src in (inp, inp2):
+        x_s.copy_(src["x"])
+        l_s.copy_(src["logits"])
+        graph.replay()
+        torch.cuda.synchronize()
+        eager = B.moe_forward(src["x"], src["logits"], wts, cfg.k, gs_h)
         assert B.nvfp4moe_last_device_status() == 0
         assert torch.equal(y_s, eager)
 

@@ -122,6 +122,44 @@ def test_moe_edge_shapes():
         assert cosine(got, ref["y"]) >= 0.9995
 
 
+def test_moe_random_shapes_sweep():
+    """Seeded random shapes through the whole forward (T from 1 to ~700, K and I
+    multiples of 128 and 64 with ragged 512-element chunks, E from k to 64, k
+    from 1 to 8), every token against the oracle; each shape also with the 2-SM
+    pair GEMMs (used where the weight tiles are whole 256-row tiles), which
+    must give the same bits as the default kernel."""
+    rng = np.random.default_rng(2024)
+    for case in range(6):
+        k = int(rng.integers(1, 9))
+        E = int(rng.integers(max(k, 2), 65))
+        tier = case % 3
+        T = 1 if tier == 0 else int(rng.integers(2, 64)) if tier == 1 else int(rng.integers(64, 700))
+        K = int(rng.choice([128, 256, 384, 640, 1024]))
+        I = int(rng.choice([64, 128, 192, 320]))
+        cfg = W.MoEConfig("sweep", T=T, K=K, I=I, E=E, k=k, gs_h=336.0)
+        g = torch.Generator(device="cpu").manual_seed(1000 + case)
+        x = torch.randn(T, K, generator=g).to(torch.bfloat16)
+        logits = torch.randn(T, E, generator=g)
+        w1 = (torch.randn(E, 2 * I, K, generator=g) * 0.05).to(torch.bfloat16)
+        w2 = (torch.randn(E, K, I, generator=g) * 0.05).to(torch.bfloat16)
+        wts = B.prepare_moe_weights(w1.to(DEV), w2.to(DEV))
+        gs_h = torch.tensor([cfg.gs_h], dtype=torch.float32, device=DEV)
+        y = B.moe_forward(x.to(DEV), logits.to(DEV), wts, k, gs_h)
+        assert B.nvfp4moe_last_device_status() == 0
+        try:
+            B.nvfp4moe_set_gemm_mode(1)
+            y_pair = B.moe_forward(x.to(DEV), logits.to(DEV), wts, k, gs_h)
+        finally:
+            B.nvfp4moe_set_gemm_mode(0)
+        assert B.nvfp4moe_last_device_status() == 0
+        assert torch.equal(y, y_pair), (T, K, I, E, k)
+        xb, w1b, w2b = W.bf16_bits(x), W.bf16_bits(w1), W.bf16_bits(w2)
+        ref = O.moe_forward(xb, logits.numpy(), lambda e: w1b[e], lambda e: w2b[e], k, np.float32(cfg.gs_h))
+        got = y.float().cpu().numpy()
+        assert_close_tol(got, ref["y"], "sweep %s" % ((T, K, I, E, k),))
+        assert cosine(got, ref["y"]) >= 0.9995, (T, K, I, E, k)
+
+
 def test_moe_deterministic_and_graph_capturable():
     cfg = W.CONFIGS["tiny"]
     inp = W.moe_inputs(cfg, seed=3, device=DEV)

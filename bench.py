@@ -51,7 +51,8 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="prefill",
-                    choices=["tiny", "decode", "prefill", "skewed", "prefill_small", "decode_small", "prefill_med", "skewed_small",
+                    choices=["tiny", "decode", "prefill", "skewed", "prefill_small", "decode_small", "prefill_med", "prefill_e32",
+                             "skewed_small",
                              "dsv4_decode", "dsv4_prefill"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)

@@ -97,6 +97,10 @@ CONFIGS = {
     # profiler-sized case for the HBM-bound kernels (quantize, combine): 32768
     # routed rows, so the L2 output the combine reads (470 MB) exceeds L2
     "prefill_med": MoEConfig("prefill_med", T=4096, K=7168, I=2048, E=32, k=8, gs_h=28.0),
+    # profiler-sized case of the front at the prefill token count: 65536 routed
+    # rows (the front's quantize + scatter then runs as its own kernel) with
+    # 32 experts, ~2 GB on the device
+    "prefill_e32": MoEConfig("prefill_e32", T=8192, K=7168, I=2048, E=32, k=8, gs_h=28.0),
 }
 
 # independent sub-streams of one seed
